@@ -1,0 +1,565 @@
+#!/usr/bin/env python
+"""Benchmark of the look-ahead sparse-KV decode hot path on one GB300.
+
+Workload: the Llama-3.1-8B-shaped decode layer of "OasisKV: Scaling In-Decode
+KV Cache Beyond HBM with Lookahead Sparse Prefetching" workloads -- 32 query
+/ 8 KV heads, head_dim 128, batch 8, 32,768-token context (2,048 blocks of
+16 per KV head), 2,048-token KV budget (128 blocks), L = 4 draft tokens,
+top-K = 128, fetch ratio 0.05 (cap 7 blocks per head and step), the full
+KV cache (1 GiB) in pinned host memory, random-walk queries (sigma 0.1).
+
+One step = one pass of the whole hot path for one layer: sparse attention,
+draft scoring, top-K, capped LRU planning and the host->HBM transfer.  Four
+independent copies of the layer (distinct seeds) are cycled step after step,
+as consecutive layers of a model would be: the working set touched between
+two visits of the same copy (4 x 134 MB) is larger than L2, and the transfer
+of one layer overlaps the next layer's compute (copy stream), as in Fig. 8.
+Each layer copy replays a CUDA graph per query set; the LRU step lives in
+device memory (oasis_plan_fetch_clocked), so replays advance it.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the
+same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_kv_cache_oasis_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode tok/s at 32K ctx, 2K-token KV budget; % of HBM+host-link roofline"
+UNIT = "tok/s"
+WORKLOAD = W.LLAMA8B_LAYER
+INSTANCES = 4
+QUERY_SETS = 20          # the workload's 20 consecutive decode steps, cycled
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["oasis", "reference"], default="oasis")
+    ap.add_argument("--instances", type=int, default=INSTANCES)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="only run this many untimed graph steps (for ncu launch lists)")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- bytes
+def algorithmic_bytes(wl, n_fetch_blocks: float, valid_slots: float):
+    """Bytes the method must move per layer-step (HBM) and over the host link."""
+    U = wl.batch * wl.num_kv_heads
+    blk = wl.block_size * wl.head_dim * 2 * 2          # K + V of one block: 8 KiB
+    attn = valid_slots * blk + wl.batch * wl.num_q_heads * wl.head_dim * 2 * 2 + U * wl.slots * 4
+    score = U * wl.num_blocks * wl.head_dim * 4 + wl.batch * wl.lookahead * wl.num_q_heads * wl.head_dim * 2 \
+        + U * wl.num_blocks * 4
+    topk = U * wl.num_blocks * 4 + U * wl.top_k * 4
+    plan = U * (wl.top_k * 4 + wl.slots * 4 * 4)        # ids, maps, LRU (read + write)
+    fetch_hbm = n_fetch_blocks * blk
+    link = n_fetch_blocks * blk
+    return dict(attn=attn, score=score, topk=topk, plan=plan, fetch=fetch_hbm,
+                hbm=attn + score + topk + plan + fetch_hbm, link=link)
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def oracle_layer_step_runner(wl, layer=0, units_per_call=None):
+    """Oracle runner.  Each call runs one layer-step for `units_per_call`
+    (request, KV head) units (all of them by default), cycling over units and
+    steps; returns the fraction of a full layer-step that the call covered."""
+    import oracle
+    cfg = wl.config()
+    qseq = W.query_sequence(wl, layer)
+    k, v = W.gen_kv(wl, layer, qseq)
+    sob, bos, lu = W.initial_resident(wl, layer)
+    pk, pv = W.initial_pool(wl, k, v, bos)
+    summ = oracle.build_summaries(cfg, k)
+    U = wl.batch * wl.num_kv_heads
+    G = wl.group
+    n = U if units_per_call is None else max(1, min(U, units_per_call))
+    if n == U:
+        stepper = oracle.Stepper(cfg, k, v, summ, sob, bos, lu, pk, pv)
+    else:
+        ucfg = oracle.unit_cfg(cfg)
+        units = []
+        for u in range(U):
+            b, h = divmod(u, wl.num_kv_heads)
+            sl = lambda a: np.ascontiguousarray(a[b:b + 1, h:h + 1])
+            units.append((b, h, oracle.Stepper(ucfg, sl(k), sl(v), sl(summ), sl(sob), sl(bos), sl(lu),
+                                               sl(pk), sl(pv))))
+    state = {"t": 0, "u": 0}
+
+    def one():
+        t = state["t"]
+        q, qd = W.step_queries(wl, qseq, t % wl.steps)
+        if n == U:
+            stepper.step(t, q, qd)
+            state["t"] += 1
+            return 1.0
+        for _ in range(n):
+            if state["t"] != t:
+                t = state["t"]
+                q, qd = W.step_queries(wl, qseq, t % wl.steps)
+            b, h, st = units[state["u"]]
+            st.step(t, np.ascontiguousarray(q[b:b + 1, h * G:(h + 1) * G]),
+                    np.ascontiguousarray(qd[b:b + 1, :, h * G:(h + 1) * G]))
+            state["u"] += 1
+            if state["u"] == U:
+                state["u"] = 0
+                state["t"] += 1
+        return n / U
+    return one
+
+
+def reference_arm(args):
+    """The CPU oracle, as it stands, on the same workload and metric.  Each
+    step is a bounded sample of a layer-step: as many (request, KV head) units
+    as fit a budget that keeps the whole run within a few minutes."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    wl = WORKLOAD
+    probe = oracle_layer_step_runner(wl, units_per_call=1)
+    probe()
+    t0 = time.perf_counter()
+    probe()
+    t_unit = time.perf_counter() - t0
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    units = max(1, min(wl.batch * wl.num_kv_heads, int(budget / max(t_unit, 1e-6))))
+    one = oracle_layer_step_runner(wl, units_per_call=units)
+    for _ in range(args.warmup):
+        one()
+    frac = 0.0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        frac += one()
+    dt = time.perf_counter() - t0
+    val = wl.batch * frac / dt
+    line = {"metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": wl.name, "global_batch": wl.batch, "seq_len": wl.ctx_tokens,
+                       "kv_budget_tokens": wl.kv_budget_tokens, "layers": 1,
+                       "parallelism": "replicas", "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"each step: {units} of the 64 (request, KV head) units of one "
+                                       "layer-step, single-threaded C oracle, double accumulation"},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(seconds: float):
+    wl = WORKLOAD
+    one = oracle_layer_step_runner(wl)
+    one()  # first step pays the one-off costs
+    n, t0 = 0, time.perf_counter()
+    while True:
+        one()
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds or n >= 50:
+            break
+    return {"value": wl.batch * n / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} full layer-steps of {wl.name} (all 64 units), single-threaded C oracle"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's
+    sources are unchanged since it was taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)[kernel]
+        if d["source_digest"] != source_digest(d["sources"]):
+            return None
+        return float(d["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def gpu_arm(args):
+    import torch
+    import torch.distributed as dist
+
+    from sparse_kv_cache_oasis_gb300 import binding as ob
+    from sparse_kv_cache_oasis_gb300.layer import LayerState, bits_to_bf16
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    ob.lib()
+    wl = WORKLOAD.with_(steps=QUERY_SETS)
+    n_inst = args.instances
+    dev = torch.device("cuda", local)
+
+    # ---- layer copies (set-up, untimed)
+    layers, qd_dev, q_dev, q_host, qd_host = [], [], [], [], []
+    for i in range(n_inst):
+        qseq = W.query_sequence(wl, i)
+        k, v = W.gen_kv(wl, i, qseq)
+        sob, bos, lu = W.initial_resident(wl, i)
+        layers.append(LayerState(wl, bits_to_bf16(k), bits_to_bf16(v), sob, bos, lu, device=str(dev)))
+        del k, v
+        qs, qds, hq, hqd = [], [], [], []
+        for t in range(QUERY_SETS):
+            q, qd = W.step_queries(wl, qseq, t)
+            hq.append(bits_to_bf16(q).pin_memory())
+            hqd.append(bits_to_bf16(qd).pin_memory())
+            qs.append(hq[-1].to(dev))
+            qds.append(hqd[-1].to(dev))
+        q_dev.append(qs)
+        qd_dev.append(qds)
+        q_host.append(hq)
+        qd_host.append(hqd)
+    torch.cuda.synchronize()
+
+    compute = torch.cuda.Stream(device=dev)
+    copy = torch.cuda.Stream(device=dev, priority=-1)
+    out_host = [torch.empty_like(L.out, device="cpu").pin_memory() for L in layers]
+    q_in = [torch.empty_like(q_dev[i][0]) for i in range(n_inst)]
+    qd_in = [torch.empty_like(qd_dev[i][0]) for i in range(n_inst)]
+
+    def enqueue(s, prev_fetch: bool, host_io: bool):
+        """Layer-step s (copy s % n, query set (s // n) % 20); with prev_fetch
+        the transfer of step s-1 runs on the copy stream beside it."""
+        i, qi = s % n_inst, (s // n_inst) % QUERY_SETS
+        L = layers[i]
+        if prev_fetch:
+            ev = torch.cuda.Event()
+            ev.record(compute)
+            copy.wait_event(ev)
+            layers[(s - 1) % n_inst].fetch(copy)
+            done = torch.cuda.Event()
+            done.record(copy)
+        if host_io:
+            q_in[i].copy_(q_host[i][qi], non_blocking=True)
+            qd_in[i].copy_(qd_host[i][qi], non_blocking=True)
+            q, qd = q_in[i], qd_in[i]
+        else:
+            q, qd = q_dev[i][qi], qd_dev[i][qi]
+        L.attention(q, compute)
+        L.predict_clocked(qd, compute)
+        if host_io:
+            out_host[i].copy_(L.out, non_blocking=True)
+        if prev_fetch:
+            compute.wait_event(done)
+
+    def trailing_fetch(s):
+        ev = torch.cuda.Event()
+        ev.record(compute)
+        copy.wait_event(ev)
+        layers[s % n_inst].fetch(copy)
+        done = torch.cuda.Event()
+        done.record(copy)
+        compute.wait_event(done)
+
+    # ---- warm the library (first calls set up per-device state), then capture graphs
+    with torch.cuda.stream(compute):
+        for s in range(2 * n_inst):
+            enqueue(s, prev_fetch=s > 0, host_io=False)
+        trailing_fetch(2 * n_inst - 1)
+    torch.cuda.synchronize()
+    period = n_inst * QUERY_SETS
+    graphs = {}
+
+    def graph_for(s, prev_fetch, host_io):
+        key = (s % period, prev_fetch, host_io)
+        if key not in graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=compute):
+                enqueue(s, prev_fetch, host_io)
+            graphs[key] = g
+        return graphs[key]
+
+    def run_steps(s0, n, host_io=False):
+        """Replays steps s0..s0+n-1 then the trailing transfer of the last one."""
+        with torch.cuda.stream(compute):
+            for s in range(s0, s0 + n):
+                graph_for(s, prev_fetch=s > s0, host_io=host_io).replay()
+            trailing_fetch(s0 + n - 1)
+
+    # capture every graph the runs below need, outside the timed regions
+    for s in range(period):
+        graph_for(s, True, False)
+        graph_for(s, False, False)
+        if not args.no_e2e:
+            graph_for(s, True, True)
+            graph_for(s, False, True)
+    torch.cuda.synchronize()
+
+    if args.profile_steps:
+        run_steps(0, args.profile_steps)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_steps": args.profile_steps}), flush=True)
+        return
+
+    # ---- warm-up and timed region
+    s = 0
+    run_steps(s, args.warmup)
+    s += args.warmup
+    torch.cuda.synchronize()
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    gpu_index = int(vis.split(",")[local]) if vis and vis.split(",")[local].strip().isdigit() else local
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+    # load soak: the sampler sees the GPU under this same work for ~0.6 s
+    # before and through the timed region
+    w0 = time.perf_counter()
+    while time.perf_counter() - w0 < 0.6:
+        run_steps(s, 2000)
+        s += 2000
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(compute)
+    run_steps(s, args.steps)
+    t1.record(compute)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    s += args.steps
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_per_step = ms / args.steps
+    value = world * wl.batch / (ms_per_step * 1e-3)
+
+    # ---- per-kernel timing: a CUDA graph of 8 launches of one kernel over the
+    # layer copies (cold L2), bracketed by events on the launching stream
+    def kernel_graph(kind):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=compute):
+            for r in range(8):
+                i = r % n_inst
+                L = layers[i]
+                if kind == "attn":
+                    L.attention(q_dev[i][0], compute)
+                elif kind == "score":
+                    ob.oasis_score_blocks(L.cfg, qd_dev[i][0], L.summ, L.scores, compute)
+                elif kind == "topk":
+                    ob.oasis_select_topk(L.cfg, L.scores, L.topk, compute)
+        return g
+
+    kinds = ["attn", "score", "topk"]
+    mean_ms = {}
+    for kind in kinds:
+        g = kernel_graph(kind)
+        with torch.cuda.stream(compute):
+            g.replay()
+        torch.cuda.synchronize()
+        vals = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(compute)
+            with torch.cuda.stream(compute):
+                g.replay()
+            b.record(compute)
+            torch.cuda.synchronize()
+            vals.append(a.elapsed_time(b) / 8)
+        mean_ms[kind] = statistics.mean(vals)
+        del g
+    # transfer volume and working-set occupancy over further (untimed) steps
+    fetched, valid = [], []
+    for r in range(n_inst * 10):
+        run_steps(s, 1)
+        s += 1
+        torch.cuda.synchronize()
+        L = layers[(s - 1) % n_inst]
+        fetched.append(int(L.n_fetch.sum().item()))
+        valid.append(int((L.block_of_slot >= 0).sum().item()))
+    n_fetch_avg = statistics.mean(fetched)
+    valid_avg = statistics.mean(valid)
+    by = algorithmic_bytes(wl, n_fetch_avg, valid_avg)
+    peak, peak_kind = measured_peaks()
+    dominant = max(["attn", "score"], key=lambda k: mean_ms[k])
+    kname = {"attn": "attn_kernel", "score": "score_kernel"}[dominant]
+    achieved = by[dominant] / (mean_ms[dominant] * 1e-3) / 1e9
+    traffic = committed_traffic(kname)
+
+    # ---- host link peak (pinned cudaMemcpyAsync), for the step roofline
+    hb = torch.empty(256 << 20, dtype=torch.uint8).pin_memory()
+    db = torch.empty_like(hb, device=dev)
+    best = 1e9
+    for _ in range(4):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        db.copy_(hb, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        best = min(best, a.elapsed_time(b))
+    link_gbs = hb.numel() / (best * 1e-3) / 1e9
+    del hb, db
+    t_roof = max(by["hbm"] / (peak * 1e9), by["link"] / (link_gbs * 1e9))
+    step_frac = t_roof / (ms_per_step * 1e-3)
+
+    # ---- end to end: inputs copied in from pinned host, output read back, every step
+    e2e = None
+    if not args.no_e2e:
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = args.steps
+        w0 = time.perf_counter()
+        e0.record(compute)
+        run_steps(s, n_e2e, host_io=True)
+        e1.record(compute)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - w0
+        s += n_e2e
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            tt = torch.tensor([ems], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ems = float(tt.item())
+        q_bytes = q_host[0][0].numel() * 2 + qd_host[0][0].numel() * 2
+        e2e = {"value": world * wl.batch / (ems / n_e2e * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": q_bytes, "d2h_bytes_per_step": out_host[0].numel() * 2,
+               "wall_s": wall}
+
+    errs = ob.oasis_device_errors()
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {
+                "workload": wl.name, "global_batch": wl.batch * world, "seq_len": wl.ctx_tokens,
+                "kv_budget_tokens": wl.kv_budget_tokens, "lookahead": wl.lookahead,
+                "top_k": wl.top_k, "fetch_ratio": wl.fetch_ratio, "fetch_cap": ob.oasis_fetch_cap(wl),
+                "layers": 1, "layer_copies_cycled": n_inst, "parallelism": f"replicas x{world}",
+                "l2": f"inputs larger than L2: {n_inst} layer copies of {by['hbm'] / 1e6:.0f} MB cycled",
+                "tok_s_if_32_layers": value / 32,
+                "graphs": "one CUDA graph per (layer copy, query set); LRU step in device memory"},
+            "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
+                         "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
+                         "bytes_per_launch": by[dominant], "ms_per_launch": mean_ms[dominant]},
+            "step_roofline": {"t_roof_us": t_roof * 1e6, "t_step_us": ms_per_step * 1e3,
+                              "frac": step_frac, "hbm_bytes": by["hbm"], "link_bytes": by["link"],
+                              "hbm_peak_gbs": peak, "link_peak_gbs": link_gbs,
+                              "fetched_blocks_per_step": n_fetch_avg},
+            "kernels_ms": mean_ms,
+            "kernel_gbs": {k: by[k] / (mean_ms[k] * 1e-3) / 1e9 for k in kinds},
+            "gpu_launches": args.steps * 5,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "device_errors": errs,
+        }
+        print(json.dumps(line), flush=True)
+    for L in layers:
+        L.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+    gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

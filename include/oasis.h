@@ -1,0 +1,223 @@
+/*
+ * oasis.h -- C ABI of liboasis, the GB300 (sm_103a) decode hot path of
+ * look-ahead sparse KV prefetching.
+ *
+ * Method: "OasisKV: Scaling In-Decode KV Cache Beyond HBM with Lookahead
+ * Sparse Prefetching" (arXiv:2608.08097; cited below as [OasisKV] with the
+ * figure, table or step of its summary page).  The full KV cache of every
+ * layer lives in pinned host memory; each (request, KV head) keeps a bounded
+ * working set of S = kv_budget_tokens / block_size KV blocks in HBM
+ * ([OasisKV] Fig. 7 left, Fig. 9).  Once per layer and decode step:
+ *
+ *   oasis_sparse_decode_attn   attention over the working set      (Fig. 7 right)
+ *   oasis_score_blocks         draft queries scan compressed keys  (Fig. 7 right)
+ *   oasis_select_topk          top-K blocks per KV head            (diagram step 2)
+ *   oasis_plan_fetch           diff vs. working set, capped LRU    (diagram step 3, Tab. 2)
+ *   oasis_fetch_blocks         host -> HBM transfer, copy stream   (diagram step 4, Fig. 8)
+ *
+ * Conventions
+ *   - All pointers except `cfg` and the outputs of the query functions are
+ *     DEVICE-accessible addresses.  `host_k`/`host_v` point to pinned host
+ *     memory mapped into the device address space (cudaHostAlloc with
+ *     cudaHostAllocMapped, or cudaHostRegister + cudaHostGetDevicePointer).
+ *   - bf16 tensors are passed as `uint16_t*` holding bf16 bit patterns.
+ *   - Streams are `cudaStream_t` values passed as `void*` (NULL = legacy
+ *     default stream).  Every call only enqueues work on the stream it is
+ *     given and returns; ordering across streams is the caller's (events).
+ *   - The caller owns every buffer.  The library allocates no device or host
+ *     memory, except a few bytes of per-device state (a device error word)
+ *     created on the first call on each device.
+ *   - Arguments are validated before anything is launched.  Invalid ones
+ *     return OASIS_ERR_INVALID_ARG (or OASIS_ERR_UNSUPPORTED for legal but
+ *     unimplemented shapes) and launch nothing.  A failed launch returns
+ *     OASIS_ERR_CUDA.  Problems only visible on the device (an out-of-range
+ *     id inside a device array, a bounded wait that ran out) never trap: the
+ *     kernel skips the offending access and sets a bit in the per-device
+ *     error word, read with oasis_device_errors().
+ *
+ * Layouts (row-major; B batch, Hq query heads, Hkv KV heads, G = Hq/Hkv,
+ * D = head_dim = 128, bs = block_size = 16, NB = num_blocks, L = lookahead,
+ * K = top_k, S = slots, cap = oasis_fetch_cap(cfg); query head h*G+g reads
+ * KV head h):
+ *   host K, V       [B][Hkv][NB][bs][D]  bf16  full cache, pinned host
+ *   summ            [B][Hkv][NB][D]      fp32  compressed keys (block means)
+ *   q_draft         [B][L][Hq][D]        bf16  draft-token queries
+ *   scores          [B][Hkv][NB]         fp32
+ *   topk_ids        [B][Hkv][K]          int32 in priority order
+ *   slot_of_block   [B][Hkv][NB]         int32 working-set slot, -1 = absent
+ *   block_of_slot   [B][Hkv][S]          int32 block in the slot, -1 = empty
+ *   last_used       [B][Hkv][S]          int32 step of last use, -1 = never
+ *   fetch_block, fetch_slot, evict_block [B][Hkv][max(cap,1)] int32, -1 padded
+ *   n_fetch, n_evict [B][Hkv]            int32
+ *   pool K, V       [B][Hkv][S][bs][D]   bf16  working set in HBM
+ *   q               [B][Hq][D]           bf16  decode query
+ *   out             [B][Hq][D]           bf16
+ */
+#ifndef OASIS_H
+#define OASIS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    OASIS_OK = 0,
+    OASIS_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or configuration */
+    OASIS_ERR_UNSUPPORTED = 2,  /* legal shape this build does not implement */
+    OASIS_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    OASIS_ERR_TIMEOUT = 4       /* oasis_stream_wait ran out of time */
+} oasis_status_t;
+
+/* Bits of the per-device error word (oasis_device_errors). */
+#define OASIS_DEVERR_FETCH_RANGE  0x1u  /* fetch list entry out of range; copy skipped */
+#define OASIS_DEVERR_PLAN_STATE   0x2u  /* inconsistent working-set map; (b,h) left unchanged */
+#define OASIS_DEVERR_TOPK_IDS     0x4u  /* top-K id out of range or repeated; (b,h) left unchanged */
+#define OASIS_DEVERR_WAIT_TIMEOUT 0x8u  /* a bounded device wait gave up; outputs invalid */
+#define OASIS_DEVERR_SLOT_RANGE   0x10u /* block_of_slot entry >= NB; slot skipped */
+
+/* Per-layer problem description ([OasisKV] diagram steps 2-3, Tab. 1-2):
+ * block size, KV budget, look-ahead tokens, top-K and fetch ratio. */
+typedef struct {
+    int32_t batch;             /* B requests */
+    int32_t num_q_heads;       /* Hq */
+    int32_t num_kv_heads;      /* Hkv; Hq % Hkv == 0 */
+    int32_t head_dim;          /* D; this build: 128 */
+    int32_t block_size;        /* tokens per KV block; this build: 16 */
+    int32_t num_blocks;        /* NB context blocks per (request, KV head) */
+    int32_t kv_budget_tokens;  /* working-set budget; S = kv_budget_tokens / block_size */
+    int32_t lookahead;         /* L draft tokens */
+    int32_t top_k;             /* K predicted blocks per KV head, K <= S, K <= NB */
+    float   fetch_ratio;       /* per-step fetch cap = ceil(ratio*S); <0 or >=1: cap = K */
+    int32_t sink_blocks;       /* blocks [0, sink) are always predicted */
+    int32_t local_blocks;      /* the last `local` blocks are always predicted */
+} oasis_config_t;
+
+/* Checks a configuration without launching anything.  OASIS_OK,
+ * OASIS_ERR_INVALID_ARG or OASIS_ERR_UNSUPPORTED.  Limits of this build:
+ * head_dim 128, block_size 16, G <= 8, L*G <= 64, S <= 1024, K <= 1024,
+ * NB <= 32768, B*Hkv <= 65535, (sink + local) <= K. */
+oasis_status_t oasis_validate_config(const oasis_config_t* cfg);
+
+/* Blocks fetched at most per (request, KV head) and step ([OasisKV] Tab. 2:
+ * the fetch ratio bounds the blocks fetched per step).  The ratio applies to
+ * the budget in blocks: cap = ceil(ratio * S - 1e-6) in double, clamped to
+ * [0, K]; a ratio < 0 or >= 1 ("fetch all") gives K.  Returns -1 for an
+ * invalid configuration. */
+int32_t oasis_fetch_cap(const oasis_config_t* cfg);
+
+/* Compressed keys ([OasisKV] Fig. 7 left): summ[b,h,j,:] = fp32 mean of the
+ * bs keys of block j, the sum taken exactly and rounded once.  Set-up work
+ * (admission), not part of the per-step path.  `k` may be a device buffer or
+ * mapped pinned host memory, 16-byte aligned; `summ` 16-byte aligned. */
+oasis_status_t oasis_build_summaries(const oasis_config_t* cfg, const uint16_t* k,
+                                     float* summ, void* stream);
+
+/* Look-ahead scoring ([OasisKV] Fig. 7 right; 'What they did' item 2):
+ * scores[b,h,j] = max over l < L, g < G of  q_draft[b,l,h*G+g,:] . summ[b,h,j,:].
+ * Tensor-core contraction with fp32 accumulation; the fp32 summary enters as
+ * a two-term tf32 split (tf32 head plus tf32-rounded residual, about 2^-22
+ * relative per term), so the result is within a few fp32 ulps of the exact
+ * value.  q_draft and summ 16-byte aligned. */
+oasis_status_t oasis_score_blocks(const oasis_config_t* cfg, const uint16_t* q_draft,
+                                  const float* summ, float* scores, void* stream);
+
+/* Per-KV-head top-K ([OasisKV] diagram step 2, Fig. 4).  Forced blocks (sink
+ * and local window) come first in ascending id and count toward K; the other
+ * K - |forced| are the highest scores, equal scores to the lower id, listed
+ * by (score descending, id ascending).  The list order is the fetch priority
+ * used by oasis_plan_fetch.  Scores must not be NaN (-0.0 equals +0.0). */
+oasis_status_t oasis_select_topk(const oasis_config_t* cfg, const float* scores,
+                                 int32_t* topk_ids, void* stream);
+
+/* Selection with capped eviction ([OasisKV] diagram step 3; Tab. 2 "LRU
+ * eviction"; Fig. 9 head-wise block map).  Per (b,h), with P = topk_ids and R
+ * the resident blocks:
+ *   1. blocks of P already in R are used at `step` (last_used = step);
+ *   2. the first n = min(|P \ R|, cap) missing blocks in list order are fetched;
+ *   3. e = max(0, |R| + n - S) victims leave R \ P, least recently used first,
+ *      equal times by lower block id;
+ *   4. free slots (empty, then freed; ascending slot index) are paired with
+ *      the fetched blocks in ascending block id; they get last_used = step.
+ * The three state arrays are updated in place.  Outputs are sorted by block
+ * id and padded with -1.  The caller must not run this while an attention
+ * call still reads the same block_of_slot, nor fetch into the pool until the
+ * attention over the old working set has finished (victim slots are reused). */
+oasis_status_t oasis_plan_fetch(const oasis_config_t* cfg, const int32_t* topk_ids,
+                                int32_t step, int32_t* slot_of_block,
+                                int32_t* block_of_slot, int32_t* last_used,
+                                int32_t* fetch_block, int32_t* fetch_slot,
+                                int32_t* evict_block, int32_t* n_fetch,
+                                int32_t* n_evict, void* stream);
+
+/* oasis_plan_fetch with the step kept in device memory: clock is [B][Hkv]
+ * int32; each (b,h) plans at step clock[b,h] and the call then advances it by
+ * one.  With every clock equal to t on entry the result is that of
+ * oasis_plan_fetch(..., step = t, ...).  No host value changes from one
+ * decode step to the next, so a captured CUDA graph of the layer step can be
+ * replayed step after step. */
+oasis_status_t oasis_plan_fetch_clocked(const oasis_config_t* cfg, const int32_t* topk_ids,
+                                        int32_t* clock, int32_t* slot_of_block,
+                                        int32_t* block_of_slot, int32_t* last_used,
+                                        int32_t* fetch_block, int32_t* fetch_slot,
+                                        int32_t* evict_block, int32_t* n_fetch,
+                                        int32_t* n_evict, void* stream);
+
+/* KV transfer ([OasisKV] diagram step 4, Fig. 8): for every r < n_fetch[b,h],
+ * copies block fetch_block[b,h,r] of host K and V into slot fetch_slot[b,h,r]
+ * of the pools.  A gather kernel reads the mapped pinned host memory directly
+ * (zero-copy over the host link); meant for a dedicated copy stream so that it
+ * overlaps compute.  All of host_k, host_v, pool_k, pool_v 16-byte aligned. */
+oasis_status_t oasis_fetch_blocks(const oasis_config_t* cfg, const uint16_t* host_k,
+                                  const uint16_t* host_v, const int32_t* fetch_block,
+                                  const int32_t* fetch_slot, const int32_t* n_fetch,
+                                  uint16_t* pool_k, uint16_t* pool_v, void* copy_stream);
+
+/* Sparse decode attention over the working set ([OasisKV] Fig. 7 right):
+ * out[b,h*G+g,:] = softmax over every token t of every valid slot s
+ * (block_of_slot >= 0, block*bs + t < ctx_len[b]) of scale * q.k, times v.
+ * One pass, online softmax, fp32 accumulation, bf16 output; a head with no
+ * visible token outputs zeros.  ctx_len is [B] int32 or NULL (no mask).
+ * `workspace` is caller-owned device scratch of at least
+ * oasis_attn_workspace_bytes(cfg) bytes, 256-byte aligned, zero-filled once
+ * before its first use; every call leaves it ready for the next one.  Calls
+ * that share a workspace must not overlap on the GPU.  q, pools and out
+ * 16-byte aligned; scale > 0. */
+oasis_status_t oasis_sparse_decode_attn(const oasis_config_t* cfg, const uint16_t* q,
+                                        const uint16_t* pool_k, const uint16_t* pool_v,
+                                        const int32_t* block_of_slot, const int32_t* ctx_len,
+                                        float scale, uint16_t* out, void* workspace,
+                                        size_t workspace_bytes, void* stream);
+
+/* Scratch bytes oasis_sparse_decode_attn needs for `cfg` (0 on invalid cfg). */
+size_t oasis_attn_workspace_bytes(const oasis_config_t* cfg);
+
+/* Pins and maps `bytes` of existing host memory at `host` (cudaHostRegister,
+ * mapped) and returns in *dev_ptr the address kernels use to read it: the
+ * form oasis_fetch_blocks expects for host_k / host_v.  Not for the per-step
+ * path (it blocks and may be slow for large ranges). */
+oasis_status_t oasis_host_register(void* host, size_t bytes, void** dev_ptr);
+/* Undoes oasis_host_register. */
+oasis_status_t oasis_host_unregister(void* host);
+
+/* Reads the current device's error word into *flags (OASIS_DEVERR_* bits)
+ * and clears it when `clear` is non-zero.  Synchronizes the device. */
+oasis_status_t oasis_device_errors(uint32_t* flags, int32_t clear);
+
+/* Waits for `stream` with a time limit: OASIS_OK once its work is done,
+ * OASIS_ERR_TIMEOUT after `timeout_ms`, OASIS_ERR_CUDA on a CUDA error. */
+oasis_status_t oasis_stream_wait(void* stream, int32_t timeout_ms);
+
+/* Human-readable name of a status code (static string). */
+const char* oasis_status_string(oasis_status_t status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int32_t oasis_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OASIS_H */

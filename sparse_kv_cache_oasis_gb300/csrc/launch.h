@@ -1,0 +1,56 @@
+// Internal launchers of the liboasis kernels.  The C ABI (api.cu) validates
+// every argument before calling these; the launchers only size grids and
+// launch.  Each returns the cudaError_t of its launch.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/oasis.h"
+
+namespace oasis {
+
+// Per-device facts the launchers need (filled once per device by api.cu).
+struct DeviceInfo {
+  int sm_count = 0;
+  int score_ctas_per_sm = 0;
+  int attn_ctas_per_sm = 0;
+  uint32_t* err = nullptr;  // device error word
+};
+
+// Derived sizes of one configuration.
+struct Shape {
+  int B, Hq, Hkv, G, D, bs, NB, S, L, K, cap, sink, local;
+  int units() const { return B * Hkv; }
+};
+
+cudaError_t launch_build_summaries(const Shape& s, const uint16_t* k, float* summ,
+                                   cudaStream_t st, const DeviceInfo& di);
+cudaError_t launch_score_blocks(const Shape& s, const uint16_t* q_draft, const float* summ,
+                                float* scores, cudaStream_t st, const DeviceInfo& di);
+cudaError_t launch_select_topk(const Shape& s, const float* scores, int32_t* topk_ids,
+                               cudaStream_t st, const DeviceInfo& di);
+cudaError_t launch_plan_fetch(const Shape& s, const int32_t* topk_ids, int32_t step,
+                              int32_t* clock, int32_t* slot_of_block, int32_t* block_of_slot,
+                              int32_t* last_used, int32_t* fetch_block, int32_t* fetch_slot,
+                              int32_t* evict_block, int32_t* n_fetch, int32_t* n_evict,
+                              cudaStream_t st, const DeviceInfo& di);
+cudaError_t launch_fetch_blocks(const Shape& s, const uint16_t* host_k, const uint16_t* host_v,
+                                const int32_t* fetch_block, const int32_t* fetch_slot,
+                                const int32_t* n_fetch, uint16_t* pool_k, uint16_t* pool_v,
+                                cudaStream_t st, const DeviceInfo& di);
+
+// Attention: the pools are read by TMA through these two tensor maps.
+size_t attn_workspace_bytes(const Shape& s);
+cudaError_t attn_configure(int device);  // one-time function attributes
+int attn_ctas_per_sm();
+cudaError_t launch_sparse_decode_attn(const Shape& s, const uint16_t* q,
+                                      const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                      const int32_t* block_of_slot, const int32_t* ctx_len,
+                                      float scale, uint16_t* out, void* workspace,
+                                      cudaStream_t st, const DeviceInfo& di);
+int score_ctas_per_sm();
+
+}  // namespace oasis

@@ -1,0 +1,120 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments before launching anything."""
+import ctypes as C
+import os
+import subprocess
+
+import pytest
+import torch
+
+from sparse_kv_cache_oasis_gb300 import binding as ob
+from sparse_kv_cache_oasis_gb300 import workloads as W
+
+import oracle
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(ob.LIB_PATH):
+        from sparse_kv_cache_oasis_gb300 import build
+        build.build()
+    return ob.lib()
+
+
+def test_exports_every_header_symbol(lib):
+    names = ob.header_symbols()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", ob.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    assert set(names) <= exported
+    # the hot-path entry points named by the method's pipeline
+    for n in ("oasis_score_blocks", "oasis_select_topk", "oasis_plan_fetch", "oasis_fetch_blocks",
+              "oasis_sparse_decode_attn"):
+        assert n in names
+
+
+def test_library_links_no_oracle_and_no_torch(lib):
+    out = subprocess.run(["nm", "-D", ob.LIB_PATH], capture_output=True, text=True).stdout
+    assert "orc_" not in out
+    deps = subprocess.run(["ldd", ob.LIB_PATH], capture_output=True, text=True).stdout
+    assert "torch" not in deps and "oracle" not in deps
+
+
+def test_status_strings_and_version(lib):
+    assert ob.oasis_status_string(ob.OASIS_OK) == "OASIS_OK"
+    assert ob.oasis_status_string(ob.OASIS_ERR_TIMEOUT) == "OASIS_ERR_TIMEOUT"
+    assert ob.oasis_version() >= 100
+
+
+@pytest.mark.parametrize("wl", [W.TINY, W.LLAMA8B_LAYER, W.QWEN3_8B_STEP, W.LONG_CTX]
+                         + [W.sweep_point(r, b) for r in W.SWEEP_RATIOS for b in (1, 64)])
+def test_workloads_validate_and_cap_matches_oracle(lib, wl):
+    assert ob.oasis_validate_config(wl) == ob.OASIS_OK
+    assert ob.oasis_fetch_cap(wl) == oracle.fetch_cap(wl.config())
+    assert ob.oasis_attn_workspace_bytes(wl) > 0
+
+
+def test_cap_matches_oracle_over_ratios(lib):
+    base = W.LLAMA8B_LAYER.config()
+    for S in (16, 64, 128, 130, 1024):
+        for r in (0.0, 0.001, 0.01, 0.02, 0.05, 0.0625, 0.1, 0.2, 0.5, 0.999, 1.0, -1.0, -0.5):
+            cfg = dict(base, kv_budget_tokens=16 * S, top_k=min(128, S), fetch_ratio=r)
+            assert ob.oasis_fetch_cap(cfg) == oracle.fetch_cap(cfg), (S, r)
+
+
+def _bad_configs():
+    good = W.TINY.config()
+    yield dict(good, batch=0), ob.OASIS_ERR_INVALID_ARG
+    yield dict(good, num_q_heads=15), ob.OASIS_ERR_INVALID_ARG
+    yield dict(good, kv_budget_tokens=1000), ob.OASIS_ERR_INVALID_ARG
+    yield dict(good, top_k=65), ob.OASIS_ERR_INVALID_ARG          # K > S
+    yield dict(good, top_k=300, kv_budget_tokens=16 * 512), ob.OASIS_ERR_INVALID_ARG  # K > NB
+    yield dict(good, sink_blocks=20, local_blocks=20), ob.OASIS_ERR_INVALID_ARG  # forced > K
+    yield dict(good, fetch_ratio=float("nan")), ob.OASIS_ERR_INVALID_ARG
+    yield dict(good, head_dim=64), ob.OASIS_ERR_UNSUPPORTED
+    yield dict(good, block_size=32, kv_budget_tokens=2048), ob.OASIS_ERR_UNSUPPORTED
+    yield dict(good, num_q_heads=64), ob.OASIS_ERR_UNSUPPORTED     # G = 16
+    yield dict(good, num_blocks=40000), ob.OASIS_ERR_UNSUPPORTED
+    yield dict(good, lookahead=0), ob.OASIS_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("cfg,status", list(_bad_configs()))
+def test_bad_configs_rejected(lib, cfg, status):
+    assert ob.oasis_validate_config(cfg) == status
+
+
+def test_entry_points_reject_bad_arguments_before_launch(lib):
+    """Null and misaligned pointers and bad configurations come back as
+    OASIS_ERR_INVALID_ARG without touching the GPU (none is present here)."""
+    c = ob.OasisConfig.make(W.TINY)
+    P = C.c_void_p
+    null = P(0)
+    odd = P(0x1001)
+    ok = P(0x10000)
+    L = lib
+    assert L.oasis_build_summaries(C.byref(c), null, ok, null) == ob.OASIS_ERR_INVALID_ARG
+    assert L.oasis_score_blocks(C.byref(c), odd, ok, ok, null) == ob.OASIS_ERR_INVALID_ARG
+    assert L.oasis_select_topk(C.byref(c), ok, null, null) == ob.OASIS_ERR_INVALID_ARG
+    assert L.oasis_plan_fetch(C.byref(c), ok, 0, ok, ok, ok, ok, ok, ok, ok, P(2), null) == ob.OASIS_ERR_INVALID_ARG
+    assert L.oasis_fetch_blocks(C.byref(c), odd, ok, ok, ok, ok, ok, ok, null) == ob.OASIS_ERR_INVALID_ARG
+    ws = ob.oasis_attn_workspace_bytes(c)
+    # scale must be positive and finite; workspace large enough and 256-byte aligned
+    assert L.oasis_sparse_decode_attn(C.byref(c), ok, ok, ok, ok, null, -1.0, ok, ok, ws, null) == ob.OASIS_ERR_INVALID_ARG
+    assert L.oasis_sparse_decode_attn(C.byref(c), ok, ok, ok, ok, null, 0.1, ok, P(0x10010), ws, null) == ob.OASIS_ERR_INVALID_ARG
+    assert L.oasis_sparse_decode_attn(C.byref(c), ok, ok, ok, ok, null, 0.1, ok, ok, ws - 1, null) == ob.OASIS_ERR_INVALID_ARG
+    bad = ob.OasisConfig.make(dict(W.TINY.config(), head_dim=64))
+    assert L.oasis_score_blocks(C.byref(bad), ok, ok, ok, null) == ob.OASIS_ERR_UNSUPPORTED
+    assert L.oasis_select_topk(None, ok, ok, null) == ob.OASIS_ERR_INVALID_ARG
+    assert ob.oasis_fetch_cap(dict(W.TINY.config(), batch=0)) == -1
+    assert ob.oasis_attn_workspace_bytes(dict(W.TINY.config(), batch=0)) == 0
+
+
+def test_binding_checks_tensors(lib):
+    wl = W.TINY
+    with pytest.raises(ValueError):  # CPU tensors are refused for device arguments
+        ob.oasis_select_topk(wl, torch.zeros(1, 4, 256), torch.zeros(1, 4, 32, dtype=torch.int32))
+    with pytest.raises(TypeError):
+        ob.oasis_select_topk(wl, torch.zeros(1, 4, 256, dtype=torch.float64),
+                             torch.zeros(1, 4, 32, dtype=torch.int32))

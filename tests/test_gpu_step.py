@@ -1,0 +1,114 @@
+"""Whole layer-steps on the GPU (all five calls, compute and copy streams)
+against the oracle, over consecutive decode steps.
+
+Each GPU step is compared with the oracle run from the GPU's own pre-step
+state (working-set maps, LRU times, pools), so that a legitimate near-tie
+difference in one step cannot compound into later ones.  Attention output
+and scores are compared within the tolerances of gpu_helpers; top-K lists
+exactly or under the near-tie rule; the plan, the maps and the pools after
+the transfer exactly (the oracle plans from the GPU's top-K list).
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import (assert_attn_close, check_topk, dev_bits, oracle_unit_step, score_bound,
+                         setup_layer)
+from sparse_kv_cache_oasis_gb300 import binding as ob
+from sparse_kv_cache_oasis_gb300 import workloads as W
+from sparse_kv_cache_oasis_gb300.layer import bf16_to_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def run_and_check(wl, steps, units=None, layer=0, ctx_len=None):
+    st, k, v, qseq = setup_layer(wl, layer, ctx_len=ctx_len)
+    cfg = wl.config()
+    compute = torch.cuda.Stream()
+    copy = torch.cuda.Stream(priority=-1)
+    B, H = wl.batch, wl.num_kv_heads
+    all_units = [(b, h) for b in range(B) for h in range(H)]
+    units = all_units if units is None else units
+    summ = st.summ.cpu().numpy()
+    exemptions = 0
+    fetched = []
+    torch.cuda.synchronize()
+    for t in range(steps):
+        q, qd = W.step_queries(wl, qseq, t)
+        torch.cuda.synchronize()
+        sob, bos, lu = st.state_numpy()
+        pk, pv = bf16_to_bits(st.pool_k), bf16_to_bits(st.pool_v)
+        with torch.cuda.stream(compute):
+            dq, dqd = dev_bits(q), dev_bits(qd)
+        st.step(t, dq, dqd, compute=compute, copy=copy)
+        torch.cuda.synchronize()
+        out = bf16_to_bits(st.out)
+        scores = st.scores.cpu().numpy()
+        topk = st.topk.cpu().numpy()
+        g_sob, g_bos, g_lu = st.state_numpy()
+        g_pk, g_pv = bf16_to_bits(st.pool_k), bf16_to_bits(st.pool_v)
+        nf = st.n_fetch.cpu().numpy()
+        fetched.append(int(nf.sum()))
+        bound = score_bound(qd, summ, wl.group)
+        for (b, h) in units:
+            ref = oracle_unit_step(cfg, b, h, t, q, qd, k, v, summ, sob, bos, lu, pk, pv,
+                                   ctx_len, st.scale, gpu_topk=topk[b, h])
+            G = wl.group
+            assert_attn_close(out[b, h * G:(h + 1) * G], ref["out"], f"step {t} unit {(b, h)}")
+            assert (np.abs(scores[b, h].astype(np.float64) - ref["scores"]) <= bound[b, h]).all()
+            exemptions += check_topk(topk[b, h], ref["topk"], ref["scores"], cfg)
+            p = ref["plan"]
+            assert nf[b, h] == p["n_fetch"][0, 0]
+            assert np.array_equal(st.fetch_block.cpu().numpy()[b, h], p["fetch_block"][0, 0])
+            assert np.array_equal(st.fetch_slot.cpu().numpy()[b, h], p["fetch_slot"][0, 0])
+            assert np.array_equal(st.evict_block.cpu().numpy()[b, h], p["evict_block"][0, 0])
+            assert np.array_equal(g_sob[b, h], ref["sob"])
+            assert np.array_equal(g_bos[b, h], ref["bos"])
+            assert np.array_equal(g_lu[b, h], ref["lu"])
+            assert np.array_equal(g_pk[b, h], ref["pool_k"]) and np.array_equal(g_pv[b, h], ref["pool_v"])
+        # invariants on every unit: cap and budget
+        cap = ob.oasis_fetch_cap(wl)
+        assert (nf <= cap).all() and ((g_bos >= 0).sum(-1) <= wl.slots).all()
+    assert ob.oasis_device_errors() == 0
+    st.close()
+    return exemptions, fetched
+
+
+def test_tiny_planted_step():
+    ex, fetched = run_and_check(W.TINY, steps=1)
+    assert ex == 0
+
+
+def test_llama_layer_full_size_consecutive_steps():
+    ex, fetched = run_and_check(W.LLAMA8B_LAYER, steps=4)
+    assert ex <= 2
+
+
+def test_llama_layer_ragged_context_lengths():
+    wl = W.LLAMA8B_LAYER.with_(batch=3, steps=2)
+    ex, _ = run_and_check(wl, steps=2, ctx_len=np.asarray([32768, 20000, 513], np.int32))
+    assert ex <= 2
+
+
+def test_long_context_forced_blocks_sampled_units():
+    wl = W.LONG_CTX.with_(steps=3)
+    units = [(0, 0), (3, 5), (7, 7), (5, 2)]
+    ex, _ = run_and_check(wl, steps=3, units=units)
+    assert ex <= 1
+
+
+def test_qwen3_heavy_hitter_layer_sampled_units():
+    wl = W.QWEN3_8B_STEP.with_(steps=2)
+    units = [(0, 0), (13, 3), (31, 7)]
+    ex, _ = run_and_check(wl, steps=2, units=units, layer=5)
+    assert ex <= 1
+
+
+@pytest.mark.parametrize("ratio", [0.01, -1.0])
+def test_sweep_points_fetch_volume(ratio):
+    wl = W.sweep_point(ratio, 8).with_(steps=3)
+    ex, fetched = run_and_check(wl, steps=3, units=[(0, 0), (7, 7)])
+    cap = ob.oasis_fetch_cap(wl)
+    if ratio > 0:
+        # the capped transfer is saturated at step 0 (random initial working set)
+        assert fetched[0] == cap * wl.batch * wl.num_kv_heads
