@@ -304,77 +304,88 @@ def gpu_arm(args):
     torch.cuda.synchronize()
 
     compute = torch.cuda.Stream(device=dev)
+    pred = torch.cuda.Stream(device=dev)
     copy = torch.cuda.Stream(device=dev, priority=-1)
     out_host = [torch.empty_like(L.out, device="cpu").pin_memory() for L in layers]
     q_in = [torch.empty_like(q_dev[i][0]) for i in range(n_inst)]
     qd_in = [torch.empty_like(qd_dev[i][0]) for i in range(n_inst)]
 
-    def enqueue(s, prev_fetch: bool, host_io: bool):
-        """Layer-step s (copy s % n, query set (s // n) % 20); with prev_fetch
-        the transfer of step s-1 runs on the copy stream beside it."""
-        i, qi = s % n_inst, (s // n_inst) % QUERY_SETS
-        L = layers[i]
-        if prev_fetch:
-            ev = torch.cuda.Event()
-            ev.record(compute)
-            copy.wait_event(ev)
-            layers[(s - 1) % n_inst].fetch(copy)
-            done = torch.cuda.Event()
-            done.record(copy)
-        if host_io:
-            q_in[i].copy_(q_host[i][qi], non_blocking=True)
-            qd_in[i].copy_(qd_host[i][qi], non_blocking=True)
-            q, qd = q_in[i], qd_in[i]
-        else:
-            q, qd = q_dev[i][qi], qd_dev[i][qi]
-        L.attention(q, compute)
-        L.predict_clocked(qd, compute)
-        if host_io:
-            out_host[i].copy_(L.out, non_blocking=True)
-        if prev_fetch:
-            compute.wait_event(done)
+    def qset(s):
+        return s % n_inst, (s // n_inst) % QUERY_SETS
 
-    def trailing_fetch(s):
-        ev = torch.cuda.Event()
-        ev.record(compute)
-        copy.wait_event(ev)
-        layers[s % n_inst].fetch(copy)
-        done = torch.cuda.Event()
-        done.record(copy)
-        compute.wait_event(done)
+    def enqueue(s, s_lo, s_hi, host_io: bool):
+        """Graph body of step s (a software pipeline over the layer copies, as
+        in Fig. 8): attention of step s on `compute`; beside it, prediction
+        (scoring, top-K, plan) of step s-1 on `pred` and the transfer of step
+        s-2 on `copy`.  Only steps in [s_lo, s_hi) are issued, so the first and
+        last graphs of a run fill and drain the pipeline.  Copy s % 4 is
+        touched by nothing else inside the graph: step s-1 and s-2 use other
+        copies, and their previous transfer/plan finished in earlier graphs."""
+        fork = torch.cuda.Event()
+        fork.record(compute)
+        joins = []
+        if s_lo <= s - 1 < s_hi:
+            i1, qi1 = qset(s - 1)
+            pred.wait_event(fork)
+            qd = qd_in[i1] if host_io else qd_dev[i1][qi1]
+            layers[i1].predict_fused(qd, pred)
+            e = torch.cuda.Event()
+            e.record(pred)
+            joins.append(e)
+        if s_lo <= s - 2 < s_hi:
+            copy.wait_event(fork)
+            layers[(s - 2) % n_inst].fetch(copy)
+            e = torch.cuda.Event()
+            e.record(copy)
+            joins.append(e)
+        if s_lo <= s < s_hi:
+            i, qi = qset(s)
+            L = layers[i]
+            if host_io:
+                q_in[i].copy_(q_host[i][qi], non_blocking=True)
+                qd_in[i].copy_(qd_host[i][qi], non_blocking=True)
+                q = q_in[i]
+            else:
+                q = q_dev[i][qi]
+            L.attention(q, compute)
+            if host_io:
+                out_host[i].copy_(L.out, non_blocking=True)
+        for e in joins:
+            compute.wait_event(e)
 
-    # ---- warm the library (first calls set up per-device state), then capture graphs
+    # ---- warm the library (first calls set up per-device state)
     with torch.cuda.stream(compute):
-        for s in range(2 * n_inst):
-            enqueue(s, prev_fetch=s > 0, host_io=False)
-        trailing_fetch(2 * n_inst - 1)
+        for s_ in range(2 * n_inst + 2):
+            enqueue(s_, 0, 2 * n_inst, host_io=False)
     torch.cuda.synchronize()
     period = n_inst * QUERY_SETS
     graphs = {}
 
-    def graph_for(s, prev_fetch, host_io):
-        key = (s % period, prev_fetch, host_io)
+    def graph_for(s, a, b, host_io):
+        """Graph of step s issuing only the steps in [s + a, s + b)."""
+        key = (s % period, a, b, host_io)
         if key not in graphs:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=compute):
-                enqueue(s, prev_fetch, host_io)
+                enqueue(s, s + a, s + b, host_io)
             graphs[key] = g
         return graphs[key]
 
     def run_steps(s0, n, host_io=False):
-        """Replays steps s0..s0+n-1 then the trailing transfer of the last one."""
+        """Exactly the work of layer-steps s0..s0+n-1: n + 2 graph replays
+        (the pipeline fills in the first two and drains in the last two)."""
         with torch.cuda.stream(compute):
-            for s in range(s0, s0 + n):
-                graph_for(s, prev_fetch=s > s0, host_io=host_io).replay()
-            trailing_fetch(s0 + n - 1)
+            for s in range(s0, s0 + n + 2):
+                a, b = max(-2, s0 - s), min(1, s0 + n - s)
+                graph_for(s, a, b, host_io).replay()
 
     # capture every graph the runs below need, outside the timed regions
+    variants = [(-2, -1), (-2, 0), (-2, 1), (-1, 0), (-1, 1), (0, 1)]
     for s in range(period):
-        graph_for(s, True, False)
-        graph_for(s, False, False)
-        if not args.no_e2e:
-            graph_for(s, True, True)
-            graph_for(s, False, True)
+        for a, b in variants:
+            graph_for(s, a, b, False)
+            if not args.no_e2e:
+                graph_for(s, a, b, True)
     torch.cuda.synchronize()
 
     if args.profile_steps:
@@ -540,7 +551,7 @@ def gpu_arm(args):
                               "fetched_blocks_per_step": n_fetch_avg},
             "kernels_ms": mean_ms,
             "kernel_gbs": {k: by[k] / (mean_ms[k] * 1e-3) / 1e9 for k in kinds},
-            "gpu_launches": args.steps * 5,
+            "gpu_launches": args.steps * 4,
             "clocks": clk,
             "cpu_baseline": cpu,
             "e2e": e2e,

@@ -165,6 +165,18 @@ oasis_status_t oasis_plan_fetch_clocked(const oasis_config_t* cfg, const int32_t
                                         int32_t* evict_block, int32_t* n_fetch,
                                         int32_t* n_evict, void* stream);
 
+/* Top-K and planning of one layer-step in one launch ([OasisKV] explanatory
+ * diagram steps 2-3): the result is exactly that of oasis_select_topk
+ * followed by oasis_plan_fetch (or oasis_plan_fetch_clocked when `clock` is
+ * not NULL, in which case `step` is ignored), with the top-K list of each
+ * (request, KV head) kept on chip in between.  topk_ids is still written. */
+oasis_status_t oasis_predict_select(const oasis_config_t* cfg, const float* scores,
+                                    int32_t step, int32_t* clock, int32_t* topk_ids,
+                                    int32_t* slot_of_block, int32_t* block_of_slot,
+                                    int32_t* last_used, int32_t* fetch_block,
+                                    int32_t* fetch_slot, int32_t* evict_block,
+                                    int32_t* n_fetch, int32_t* n_evict, void* stream);
+
 /* KV transfer ([OasisKV] diagram step 4, Fig. 8): for every r < n_fetch[b,h],
  * copies block fetch_block[b,h,r] of host K and V into slot fetch_slot[b,h,r]
  * of the pools.  A gather kernel reads the mapped pinned host memory directly

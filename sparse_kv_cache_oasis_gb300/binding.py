@@ -57,6 +57,7 @@ _SIGS = {
     "oasis_select_topk": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P]),
     "oasis_plan_fetch": (C.c_int, [C.POINTER(OasisConfig), _P, C.c_int32] + [_P] * 9),
     "oasis_plan_fetch_clocked": (C.c_int, [C.POINTER(OasisConfig)] + [_P] * 11),
+    "oasis_predict_select": (C.c_int, [C.POINTER(OasisConfig), _P, C.c_int32] + [_P] * 11),
     "oasis_fetch_blocks": (C.c_int, [C.POINTER(OasisConfig)] + [_P] * 8),
     "oasis_sparse_decode_attn": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P, _P, _P, C.c_float,
                                            _P, _P, C.c_size_t, _P]),
@@ -206,6 +207,26 @@ def oasis_plan_fetch_clocked(cfg, topk_ids, clock, slot_of_block, block_of_slot,
     _check("oasis_plan_fetch_clocked", lib().oasis_plan_fetch_clocked(
         C.byref(c), _ptr(topk_ids, i32, (B, H, c.top_k), "topk_ids"),
         _ptr(clock, i32, (B, H), "clock"),
+        _ptr(slot_of_block, i32, (B, H, NB), "slot_of_block"),
+        _ptr(block_of_slot, i32, (B, H, S), "block_of_slot"),
+        _ptr(last_used, i32, (B, H, S), "last_used"),
+        _ptr(fetch_block, i32, (B, H, w), "fetch_block"), _ptr(fetch_slot, i32, (B, H, w), "fetch_slot"),
+        _ptr(evict_block, i32, (B, H, w), "evict_block"), _ptr(n_fetch, i32, (B, H), "n_fetch"),
+        _ptr(n_evict, i32, (B, H), "n_evict"), _stream(stream)))
+
+
+def oasis_predict_select(cfg, scores, step, clock, topk_ids, slot_of_block, block_of_slot,
+                         last_used, fetch_block, fetch_slot, evict_block, n_fetch, n_evict,
+                         stream=None) -> None:
+    """Top-K then plan in one launch; `clock` ([B, Hkv] int32 tensor) or None."""
+    c = OasisConfig.make(cfg)
+    B, H, Hq, NB, bs, D, S = _dims(c)
+    w = cap_width(c)
+    i32 = torch.int32
+    ck = C.c_void_p(0) if clock is None else _ptr(clock, i32, (B, H), "clock")
+    _check("oasis_predict_select", lib().oasis_predict_select(
+        C.byref(c), _ptr(scores, torch.float32, (B, H, NB), "scores"), int(step), ck,
+        _ptr(topk_ids, i32, (B, H, c.top_k), "topk_ids"),
         _ptr(slot_of_block, i32, (B, H, NB), "slot_of_block"),
         _ptr(block_of_slot, i32, (B, H, S), "block_of_slot"),
         _ptr(last_used, i32, (B, H, S), "last_used"),

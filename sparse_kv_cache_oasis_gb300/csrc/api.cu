@@ -45,6 +45,7 @@ oasis_status_t device_info(DeviceInfo* out) {
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return OASIS_ERR_CUDA;
     di.err = static_cast<uint32_t*>(p);
     if (attn_configure(dev) != cudaSuccess) return OASIS_ERR_CUDA;
+    if (score_configure() != cudaSuccess) return OASIS_ERR_CUDA;
     di.score_ctas_per_sm = score_ctas_per_sm();
     di.attn_ctas_per_sm = attn_ctas_per_sm();
     d.info = di;
@@ -238,6 +239,28 @@ oasis_status_t oasis_plan_fetch_clocked(const oasis_config_t* cfg, const int32_t
   return from_cuda(launch_plan_fetch(s, topk_ids, 0, clock, slot_of_block, block_of_slot,
                                      last_used, fetch_block, fetch_slot, evict_block, n_fetch,
                                      n_evict, static_cast<cudaStream_t>(stream), di));
+}
+
+oasis_status_t oasis_predict_select(const oasis_config_t* cfg, const float* scores,
+                                    int32_t step, int32_t* clock, int32_t* topk_ids,
+                                    int32_t* slot_of_block, int32_t* block_of_slot,
+                                    int32_t* last_used, int32_t* fetch_block,
+                                    int32_t* fetch_slot, int32_t* evict_block,
+                                    int32_t* n_fetch, int32_t* n_evict, void* stream) {
+  Shape s;
+  oasis_status_t st = make_shape(cfg, &s);
+  if (st != OASIS_OK) return st;
+  const void* ptrs[] = {scores, topk_ids, slot_of_block, block_of_slot, last_used,
+                        fetch_block, fetch_slot, evict_block, n_fetch, n_evict};
+  for (const void* p : ptrs)
+    if (!aligned(p, 4)) return OASIS_ERR_INVALID_ARG;
+  if (clock && !aligned(clock, 4)) return OASIS_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != OASIS_OK) return st;
+  return from_cuda(launch_select_and_plan(s, scores, topk_ids, step, clock, slot_of_block,
+                                          block_of_slot, last_used, fetch_block, fetch_slot,
+                                          evict_block, n_fetch, n_evict,
+                                          static_cast<cudaStream_t>(stream), di));
 }
 
 oasis_status_t oasis_fetch_blocks(const oasis_config_t* cfg, const uint16_t* host_k,

@@ -37,6 +37,12 @@ cudaError_t launch_plan_fetch(const Shape& s, const int32_t* topk_ids, int32_t s
                               int32_t* last_used, int32_t* fetch_block, int32_t* fetch_slot,
                               int32_t* evict_block, int32_t* n_fetch, int32_t* n_evict,
                               cudaStream_t st, const DeviceInfo& di);
+cudaError_t launch_select_and_plan(const Shape& s, const float* scores, int32_t* topk_ids,
+                                   int32_t step, int32_t* clock, int32_t* slot_of_block,
+                                   int32_t* block_of_slot, int32_t* last_used,
+                                   int32_t* fetch_block, int32_t* fetch_slot,
+                                   int32_t* evict_block, int32_t* n_fetch, int32_t* n_evict,
+                                   cudaStream_t st, const DeviceInfo& di);
 cudaError_t launch_fetch_blocks(const Shape& s, const uint16_t* host_k, const uint16_t* host_v,
                                 const int32_t* fetch_block, const int32_t* fetch_slot,
                                 const int32_t* n_fetch, uint16_t* pool_k, uint16_t* pool_v,
@@ -52,5 +58,6 @@ cudaError_t launch_sparse_decode_attn(const Shape& s, const uint16_t* q,
                                       float scale, uint16_t* out, void* workspace,
                                       cudaStream_t st, const DeviceInfo& di);
 int score_ctas_per_sm();
+cudaError_t score_configure();  // one-time function attributes
 
 }  // namespace oasis

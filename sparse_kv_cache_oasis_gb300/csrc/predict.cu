@@ -1,0 +1,470 @@
+// Top-K block prediction and capped-eviction planning ("OasisKV: Scaling
+// In-Decode KV Cache Beyond HBM with Lookahead Sparse Prefetching",
+// explanatory diagram steps 2-3; Fig. 4; Tab. 2 fetch cap and LRU eviction;
+// Fig. 9 head-wise GPU-slot <-> CPU-block map).
+//
+// Both steps are small integer work per (request, KV head) and bound by
+// latency, so each unit is one CTA and the code is organised to keep the
+// chain of dependent memory round trips and barriers short:
+//
+// Top-K (topk_unit): scores stay in registers as order-preserving 32-bit
+// keys (-0.0 folded onto +0.0, so the order is the fp32 order); a 4-pass MSB
+// radix select with warp-aggregated shared histograms finds the threshold;
+// equal keys are taken by ascending id; the selected blocks are compacted with
+// one atomic per warp and placed by counting larger 64-bit keys
+// (score_key << 32 | ~id), several threads per key.  Forced blocks (sink and
+// local window) come first in ascending id.  Output order: score descending,
+// id ascending -- the fetch priority.
+//
+// Plan (plan_unit): the working-set map entries are loaded up front; ids are
+// checked with a shared bitmap; LRU victims are ranked by counting smaller
+// 64-bit (last_used, block) keys; prefix sums give the fetch set and the free
+// slots; fetched blocks in ascending id take the free slots in ascending
+// order.  Results equal the plain sequential definition exactly.  Bad input
+// (id out of range or repeated, map directions disagreeing) leaves the unit
+// unchanged, reports n = e = 0 and sets an error bit.
+//
+// Three kernels: top-K alone, plan alone, and both fused in one CTA (the
+// top-K list never leaves shared memory before the plan uses it, and the map
+// loads overlap the selection).
+#include "common.cuh"
+#include "launch.h"
+
+namespace oasis {
+
+constexpr int kPredThreads = 1024;
+constexpr int kMaxK = 1024;
+constexpr int kMaxNBWords = 32768 / 32;
+
+__device__ __forceinline__ uint32_t orderable(float f) {
+  uint32_t b = __float_as_uint(f);
+  if (b == 0x80000000u) b = 0u;  // -0.0 == +0.0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+struct TopkSmem {
+  int hist[256];
+  int digit, greater, equal, count;
+  int scan[33];
+  unsigned long long keys[kMaxK];
+};
+
+struct PlanSmem {
+  unsigned long long lru_key[kMaxK];   // per slot: candidate key or ~0
+  int bos[kMaxK];                      // block of slot (updated in place)
+  int lu[kMaxK];                       // last used (updated in place)
+  unsigned int seen[kMaxNBWords];      // bitmap of predicted ids
+  int fetch[kMaxK];                    // fetched blocks, priority order
+  int free_slot[kMaxK];                // free slots, ascending
+  int victim[kMaxK];                   // victim blocks, LRU order
+  int inp[kMaxK];                      // slot holds a predicted block
+  int scan[33];
+  int bad;
+};
+
+// Writes the unit's top-K list (priority order) to `out_smem` (K ints) and,
+// if out_global is not null, to global memory.  All threads must call it.
+template <int ITEMS>
+__device__ void topk_unit(const float* __restrict__ sc, int NB, int K, int sink, int local,
+                          int* out_smem, int32_t* __restrict__ out_global, TopkSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int T = blockDim.x;
+  const int a = sink < NB ? sink : NB;
+  const int b0 = NB - local > 0 ? NB - local : 0;
+  const int lo = a > b0 ? a : b0;
+  const int F = a + (NB - lo);
+  const int need = K - F;
+  for (int i = tid; i < F && i < K; i += T) {
+    const int id = i < a ? i : lo + (i - a);
+    out_smem[i] = id;
+    if (out_global) out_global[i] = id;
+  }
+  if (need <= 0) {
+    __syncthreads();
+    return;
+  }
+  uint32_t key[ITEMS];
+  bool valid[ITEMS];
+#pragma unroll
+  for (int it = 0; it < ITEMS; ++it) {
+    const int j = tid + it * T;
+    valid[it] = j < NB && !(j < a || j >= lo);
+    key[it] = valid[it] ? orderable(__ldcg(sc + j)) : 0u;
+  }
+  uint32_t prefix = 0u, mask = 0u;
+  int remaining = need;
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < 256; i += T) sm.hist[i] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+      const bool part = valid[it] && (key[it] & mask) == prefix;
+      const int bin = part ? static_cast<int>((key[it] >> shift) & 255u) : 256;
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      if (part && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[bin], __popc(peers));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int c[8], lsum = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        c[k] = sm.hist[lane * 8 + k];
+        lsum += c[k];
+      }
+      int incl = lsum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += y;
+      }
+      int running = incl - lsum;
+#pragma unroll
+      for (int k = 7; k >= 0; --k) {
+        if (running < remaining && running + c[k] >= remaining) {
+          sm.digit = lane * 8 + k;
+          sm.greater = running;
+          sm.equal = c[k];
+        }
+        running += c[k];
+      }
+    }
+    __syncthreads();
+    prefix |= static_cast<uint32_t>(sm.digit) << shift;
+    mask |= 255u << shift;
+    remaining -= sm.greater;
+  }
+  const int n_equal = sm.equal;
+  int eq_rank[ITEMS];
+#pragma unroll
+  for (int it = 0; it < ITEMS; ++it) eq_rank[it] = 0;
+  if (n_equal > remaining) {  // ties at the threshold: lowest ids first
+    int base = 0;
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+      int tot;
+      const int e = valid[it] && key[it] == prefix;
+      eq_rank[it] = base + block_exclusive_scan(e, sm.scan, &tot);
+      base += tot;
+    }
+  }
+  if (tid == 0) sm.count = 0;
+  __syncthreads();
+#pragma unroll
+  for (int it = 0; it < ITEMS; ++it) {
+    const int j = tid + it * T;
+    const bool sel =
+        valid[it] && (key[it] > prefix || (key[it] == prefix && eq_rank[it] < remaining));
+    const unsigned bal = __ballot_sync(0xffffffffu, sel);
+    int base = 0;
+    if (lane == 0 && bal) base = atomicAdd(&sm.count, __popc(bal));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (sel) {
+      const int pos = base + __popc(bal & ((1u << lane) - 1u));
+      if (pos < kMaxK)
+        sm.keys[pos] = (static_cast<unsigned long long>(key[it]) << 32) |
+                       static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(j));
+    }
+  }
+  __syncthreads();
+  // rank = number of larger keys; tpk threads per key share the comparisons
+  int tpk = 1;
+  while (tpk < 32 && need * tpk * 2 <= T) tpk *= 2;
+  for (int i0 = 0; i0 < need; i0 += T / tpk) {
+    const int i = i0 + tid / tpk, sub = tid % tpk;
+    unsigned long long my = 0ull;
+    int r = 0;
+    if (i < need) {
+      my = sm.keys[i];
+      for (int k = sub; k < need; k += tpk) r += sm.keys[k] > my;
+    }
+    for (int o = 1; o < tpk; o <<= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    if (i < need && sub == 0) {
+      const int id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(my & 0xFFFFFFFFull));
+      out_smem[F + r] = id;
+      if (out_global) out_global[F + r] = id;
+    }
+  }
+  __syncthreads();
+}
+
+// Per-thread view of the unit's working-set map, loaded before the plan.
+struct SlotView {
+  int bos;   // block in slot tid (tid < S), else -1
+  int lu;    // last used of slot tid
+  int chk;   // slot_of_block[bos] when the slot is valid, for the map check
+};
+
+__device__ __forceinline__ SlotView load_slot_view(const int32_t* __restrict__ sob,
+                                                   const int32_t* __restrict__ bos,
+                                                   const int32_t* __restrict__ lu, int S, int NB) {
+  SlotView v{-1, -1, static_cast<int>(threadIdx.x)};
+  if (static_cast<int>(threadIdx.x) < S) {
+    v.bos = bos[threadIdx.x];
+    v.lu = lu[threadIdx.x];
+    if (v.bos >= 0 && v.bos < NB) v.chk = sob[v.bos];
+  }
+  return v;
+}
+
+// Plans one unit from the priority list P (shared memory, K ints).  Needs
+// blockDim.x >= max(S, K).  All threads must call it.
+__device__ void plan_unit(const int* P, const SlotView v, int32_t step, int32_t* __restrict__ clock_u,
+                          int32_t* __restrict__ sob, int32_t* __restrict__ bos,
+                          int32_t* __restrict__ lu, int32_t* __restrict__ fetch_block,
+                          int32_t* __restrict__ fetch_slot, int32_t* __restrict__ evict_block,
+                          int32_t* __restrict__ n_fetch_u, int32_t* __restrict__ n_evict_u,
+                          int NB, int S, int K, int cap, int capw, uint32_t* err, PlanSmem& sm) {
+  const int tid = threadIdx.x, T = blockDim.x;
+  if (tid == 0) sm.bad = 0;
+  for (int w = tid; w < (NB + 31) / 32; w += T) sm.seen[w] = 0u;
+  if (tid < S) sm.inp[tid] = 0;
+  __syncthreads();
+  // ids in range and distinct; both directions of the map agree
+  int p = -1, sp = -1;
+  if (tid < K) {
+    p = P[tid];
+    if (p < 0 || p >= NB) {
+      atomicOr(&sm.bad, OASIS_DEVERR_TOPK_IDS);
+    } else {
+      const unsigned bit = 1u << (p & 31);
+      if (atomicOr(&sm.seen[p >> 5], bit) & bit) atomicOr(&sm.bad, OASIS_DEVERR_TOPK_IDS);
+      sp = sob[p];
+    }
+  }
+  if (tid < S && (v.bos >= NB || (v.bos >= 0 && v.chk != tid)))
+    atomicOr(&sm.bad, OASIS_DEVERR_PLAN_STATE);
+  if (tid < S) sm.bos[tid] = v.bos;
+  __syncthreads();
+  if (tid < K && sp >= 0 && (sp >= S || sm.bos[sp] != p)) atomicOr(&sm.bad, OASIS_DEVERR_PLAN_STATE);
+  __syncthreads();
+  const int bad = sm.bad;
+  if (bad) {
+    if (tid == 0) {
+      set_error(err, static_cast<uint32_t>(bad));
+      *n_fetch_u = 0;
+      *n_evict_u = 0;
+      if (clock_u) *clock_u = step + 1;
+    }
+    for (int r = tid; r < capw; r += T) {
+      fetch_block[r] = -1;
+      fetch_slot[r] = -1;
+      evict_block[r] = -1;
+    }
+    return;
+  }
+  // 1. predicted blocks already resident are used at `step`
+  if (tid < K && sp >= 0) sm.inp[sp] = 1;
+  // 2. the first n misses in priority order are fetched
+  const int miss = (tid < K) && sp < 0;
+  int nmiss;
+  const int mrank = block_exclusive_scan(miss, sm.scan, &nmiss);  // its barriers publish inp
+  const int n = nmiss < cap ? nmiss : cap;
+  if (miss && mrank < n) sm.fetch[mrank] = p;
+  // 3. LRU victims among residents outside the prediction
+  const bool resident = tid < S && v.bos >= 0;
+  const bool cand = resident && sm.inp[tid] == 0;
+  const int nres = __syncthreads_count(resident);
+  int e = nres + n - S;
+  if (e < 0) e = 0;
+  unsigned long long mykey = ~0ull;
+  if (cand)
+    mykey = (static_cast<unsigned long long>(static_cast<uint32_t>(v.lu) ^ 0x80000000u) << 32) |
+            static_cast<uint32_t>(v.bos);
+  if (tid < S) sm.lru_key[tid] = mykey;
+  __syncthreads();
+  int victim = 0;
+  if (cand && e > 0) {
+    int rank = 0;
+#pragma unroll 8
+    for (int s2 = 0; s2 < S; ++s2) rank += sm.lru_key[s2] < mykey;
+    if (rank < e) {
+      victim = 1;
+      sm.victim[rank] = v.bos;
+    }
+  }
+  // 4. free slots (empty or freed) in ascending order
+  const int is_free = (tid < S) && (v.bos < 0 || victim);
+  int nfree;
+  const int frank = block_exclusive_scan(is_free, sm.scan, &nfree);
+  if (is_free && frank < n) sm.free_slot[frank] = tid;
+  __syncthreads();
+  // fetched blocks in ascending id take the free slots in ascending order
+  int my_blk = -1, my_slot = -1;
+  if (tid < n) {
+    my_blk = sm.fetch[tid];
+    int r = 0;
+    for (int i = 0; i < n; ++i) r += sm.fetch[i] < my_blk;
+    my_slot = sm.free_slot[r];
+    fetch_block[r] = my_blk;
+    fetch_slot[r] = my_slot;
+  }
+  if (tid < e) {
+    const int vb = sm.victim[tid];
+    int r = 0;
+    for (int i = 0; i < e; ++i) r += sm.victim[i] < vb;
+    evict_block[r] = vb;
+  }
+  for (int r = tid; r < capw; r += T) {
+    if (r >= n) {
+      fetch_block[r] = -1;
+      fetch_slot[r] = -1;
+    }
+    if (r >= e) evict_block[r] = -1;
+  }
+  // apply: victims leave, fetched blocks enter; predicted residents are used now
+  int new_bos = v.bos, new_lu = (tid < S && sm.inp[tid]) ? step : v.lu;
+  if (victim) {
+    sob[v.bos] = -1;
+    new_bos = -1;
+  }
+  if (tid < S) {
+    sm.bos[tid] = new_bos;
+    sm.lu[tid] = new_lu;
+  }
+  __syncthreads();
+  if (tid < n) {
+    sm.bos[my_slot] = my_blk;
+    sm.lu[my_slot] = step;
+    sob[my_blk] = my_slot;
+  }
+  __syncthreads();
+  if (tid < S) {
+    bos[tid] = sm.bos[tid];
+    lu[tid] = sm.lu[tid];
+  }
+  if (tid == 0) {
+    *n_fetch_u = n;
+    *n_evict_u = e;
+    if (clock_u) *clock_u = step + 1;
+  }
+}
+
+// ---------------------------------------------------------------- kernels
+template <int ITEMS>
+__global__ void __launch_bounds__(kPredThreads) topk_kernel(const float* __restrict__ scores,
+                                                            int32_t* __restrict__ topk_ids,
+                                                            int NB, int K, int sink, int local) {
+  __shared__ TopkSmem sm;
+  __shared__ int sP[kMaxK];
+  const int64_t u = blockIdx.x;
+  topk_unit<ITEMS>(scores + u * NB, NB, K, sink, local, sP, topk_ids + u * K, sm);
+}
+
+__global__ void __launch_bounds__(kPredThreads) plan_kernel(
+    const int32_t* __restrict__ topk_ids, int32_t step, int32_t* __restrict__ clock,
+    int32_t* __restrict__ slot_of_block, int32_t* __restrict__ block_of_slot,
+    int32_t* __restrict__ last_used, int32_t* __restrict__ fetch_block,
+    int32_t* __restrict__ fetch_slot, int32_t* __restrict__ evict_block,
+    int32_t* __restrict__ n_fetch, int32_t* __restrict__ n_evict, int NB, int S, int K, int cap,
+    int capw, uint32_t* err) {
+  __shared__ PlanSmem sm;
+  __shared__ int sP[kMaxK];
+  const int64_t u = blockIdx.x;
+  const int32_t st = clock ? clock[u] : step;
+  int32_t* sob = slot_of_block + u * NB;
+  const SlotView v = load_slot_view(sob, block_of_slot + u * S, last_used + u * S, S, NB);
+  for (int i = threadIdx.x; i < K; i += blockDim.x) sP[i] = topk_ids[u * K + i];
+  __syncthreads();
+  plan_unit(sP, v, st, clock ? clock + u : nullptr, sob, block_of_slot + u * S, last_used + u * S,
+            fetch_block + u * capw, fetch_slot + u * capw, evict_block + u * capw, n_fetch + u,
+            n_evict + u, NB, S, K, cap, capw, err, sm);
+}
+
+// Top-K and plan of one unit in one CTA; the map loads overlap the selection.
+template <int ITEMS>
+__global__ void __launch_bounds__(kPredThreads) topk_plan_kernel(
+    const float* __restrict__ scores, int32_t* __restrict__ topk_ids, int32_t step,
+    int32_t* __restrict__ clock, int32_t* __restrict__ slot_of_block,
+    int32_t* __restrict__ block_of_slot, int32_t* __restrict__ last_used,
+    int32_t* __restrict__ fetch_block, int32_t* __restrict__ fetch_slot,
+    int32_t* __restrict__ evict_block, int32_t* __restrict__ n_fetch,
+    int32_t* __restrict__ n_evict, int NB, int S, int K, int cap, int capw, int sink, int local,
+    uint32_t* err) {
+  __shared__ union {
+    TopkSmem topk;
+    PlanSmem plan;
+  } sm;
+  __shared__ int sP[kMaxK];
+  const int64_t u = blockIdx.x;
+  const int32_t st = clock ? clock[u] : step;
+  int32_t* sob = slot_of_block + u * NB;
+  const SlotView v = load_slot_view(sob, block_of_slot + u * S, last_used + u * S, S, NB);
+  topk_unit<ITEMS>(scores + u * NB, NB, K, sink, local, sP, topk_ids + u * K, sm.topk);
+  plan_unit(sP, v, st, clock ? clock + u : nullptr, sob, block_of_slot + u * S, last_used + u * S,
+            fetch_block + u * capw, fetch_slot + u * capw, evict_block + u * capw, n_fetch + u,
+            n_evict + u, NB, S, K, cap, capw, err, sm.plan);
+}
+
+static int threads_for(int need) {
+  int t = ((need + 31) / 32) * 32;
+  if (t < 128) t = 128;
+  return t > kPredThreads ? kPredThreads : t;
+}
+
+template <int ITEMS>
+static cudaError_t launch_topk_items(const Shape& s, const float* scores, int32_t* topk_ids,
+                                     cudaStream_t st) {
+  topk_kernel<ITEMS><<<s.units(), kPredThreads, 0, st>>>(scores, topk_ids, s.NB, s.K, s.sink, s.local);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select_topk(const Shape& s, const float* scores, int32_t* topk_ids,
+                               cudaStream_t st, const DeviceInfo&) {
+  const int items = (s.NB + kPredThreads - 1) / kPredThreads;
+  if (items <= 1) return launch_topk_items<1>(s, scores, topk_ids, st);
+  if (items <= 2) return launch_topk_items<2>(s, scores, topk_ids, st);
+  if (items <= 4) return launch_topk_items<4>(s, scores, topk_ids, st);
+  if (items <= 8) return launch_topk_items<8>(s, scores, topk_ids, st);
+  if (items <= 16) return launch_topk_items<16>(s, scores, topk_ids, st);
+  if (items <= 32) return launch_topk_items<32>(s, scores, topk_ids, st);
+  return cudaErrorInvalidValue;  // rejected by validation (NB <= 32768)
+}
+
+cudaError_t launch_plan_fetch(const Shape& s, const int32_t* topk_ids, int32_t step,
+                              int32_t* clock, int32_t* slot_of_block, int32_t* block_of_slot,
+                              int32_t* last_used, int32_t* fetch_block, int32_t* fetch_slot,
+                              int32_t* evict_block, int32_t* n_fetch, int32_t* n_evict,
+                              cudaStream_t st, const DeviceInfo& di) {
+  const int capw = s.cap > 0 ? s.cap : 1;
+  plan_kernel<<<s.units(), threads_for(s.S > s.K ? s.S : s.K), 0, st>>>(
+      topk_ids, step, clock, slot_of_block, block_of_slot, last_used, fetch_block, fetch_slot,
+      evict_block, n_fetch, n_evict, s.NB, s.S, s.K, s.cap, capw, di.err);
+  return cudaGetLastError();
+}
+
+template <int ITEMS>
+static cudaError_t launch_tp_items(const Shape& s, const float* scores, int32_t* topk_ids,
+                                   int32_t step, int32_t* clock, int32_t* sob, int32_t* bos,
+                                   int32_t* lu, int32_t* fb, int32_t* fs, int32_t* eb,
+                                   int32_t* nf, int32_t* ne, cudaStream_t st, uint32_t* err) {
+  const int capw = s.cap > 0 ? s.cap : 1;
+  topk_plan_kernel<ITEMS><<<s.units(), kPredThreads, 0, st>>>(
+      scores, topk_ids, step, clock, sob, bos, lu, fb, fs, eb, nf, ne, s.NB, s.S, s.K, s.cap,
+      capw, s.sink, s.local, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select_and_plan(const Shape& s, const float* scores, int32_t* topk_ids,
+                                   int32_t step, int32_t* clock, int32_t* slot_of_block,
+                                   int32_t* block_of_slot, int32_t* last_used,
+                                   int32_t* fetch_block, int32_t* fetch_slot,
+                                   int32_t* evict_block, int32_t* n_fetch, int32_t* n_evict,
+                                   cudaStream_t st, const DeviceInfo& di) {
+  const int items = (s.NB + kPredThreads - 1) / kPredThreads;
+#define OASIS_TP(N)                                                                           \
+  return launch_tp_items<N>(s, scores, topk_ids, step, clock, slot_of_block, block_of_slot,    \
+                            last_used, fetch_block, fetch_slot, evict_block, n_fetch, n_evict, \
+                            st, di.err)
+  if (items <= 1) OASIS_TP(1);
+  if (items <= 2) OASIS_TP(2);
+  if (items <= 4) OASIS_TP(4);
+  if (items <= 8) OASIS_TP(8);
+  if (items <= 16) OASIS_TP(16);
+  if (items <= 32) OASIS_TP(32);
+#undef OASIS_TP
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace oasis

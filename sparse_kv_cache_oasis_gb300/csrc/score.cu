@@ -14,11 +14,13 @@
 //     below the fp32 result rounding that ranking depends on;
 //   - mma.sync m16n8k8 tf32 with fp32 accumulation, one 16-row tile per 16
 //     query rows.
-// Memory path: summaries are streamed once with 16-byte evict-first loads
-// straight into the MMA fragment registers (no shared-memory staging).  The
-// contraction index is permuted so that thread (g, t) of a warp loads 16
-// contiguous bytes of block g: dims 16p+4t..16p+4t+3 serve k-steps 2p and
-// 2p+1 (A uses the same permutation, so the dot products are unchanged).
+// Memory path: summaries are streamed once with 16-byte cp.async copies into
+// a per-warp ring of kScoreStages tiles in shared memory (L1 bypassed); each
+// lane copies exactly the 8 x 16 bytes its B fragments need and reads them back
+// itself, so the ring layout [p][lane] is bank-conflict free and needs no
+// barrier.  The contraction index is permuted so that thread (g, t) of a warp
+// loads 16 contiguous bytes of block g: dims 16p+4t..16p+4t+3 serve k-steps
+// 2p and 2p+1 (A uses the same permutation, so the dot products are unchanged).
 // Each warp handles tiles of 8 consecutive blocks; the grid is sized to one
 // wave of resident CTAs.
 #include "common.cuh"
@@ -28,18 +30,120 @@ namespace oasis {
 
 constexpr int kScoreThreads = 256;
 constexpr int kScoreWarps = kScoreThreads / 32;
+constexpr int kScoreStages = 3;  // tiles of 8 blocks in flight per warp (4 KiB each)
+
+// 16-byte asynchronous global->shared copy (bypasses L1) and its group fences.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Scores of 8 blocks (one tile) from their summaries in v; writes them out.
+template <int MT>
+__device__ __forceinline__ void score_tile(const float4 (&v)[8], const float4* sQ, int lane, int g,
+                                           int t, int M, int n0, int NB, int64_t out_off,
+                                           float* out) {
+  float acc[MT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    const uint32_t hx = to_tf32(v[p].x), hy = to_tf32(v[p].y);
+    const uint32_t hz = to_tf32(v[p].z), hw = to_tf32(v[p].w);
+    const uint32_t lx = to_tf32(v[p].x - __uint_as_float(hx));
+    const uint32_t ly = to_tf32(v[p].y - __uint_as_float(hy));
+    const uint32_t lz = to_tf32(v[p].z - __uint_as_float(hz));
+    const uint32_t lw = to_tf32(v[p].w - __uint_as_float(hw));
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const float4 qa = sQ[((mt * 8 + p) * 2 + 0) * 32 + lane];
+      const float4 qb = sQ[((mt * 8 + p) * 2 + 1) * 32 + lane];
+      const uint32_t a0 = __float_as_uint(qa.x), a1 = __float_as_uint(qb.x);
+      const uint32_t a2 = __float_as_uint(qa.y), a3 = __float_as_uint(qb.y);
+      const uint32_t c0 = __float_as_uint(qa.z), c1 = __float_as_uint(qb.z);
+      const uint32_t c2 = __float_as_uint(qa.w), c3 = __float_as_uint(qb.w);
+      mma_tf32_1688(acc[mt], a0, a1, a2, a3, hx, hy);  // k-step 2p, hi
+      mma_tf32_1688(acc[mt], a0, a1, a2, a3, lx, ly);  // k-step 2p, lo
+      mma_tf32_1688(acc[mt], c0, c1, c2, c3, hz, hw);  // k-step 2p+1, hi
+      mma_tf32_1688(acc[mt], c0, c1, c2, c3, lz, lw);  // k-step 2p+1, lo
+    }
+  }
+  // max over the valid query rows (rows >= L*G are padding)
+  float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    if (16 * mt + g < M) {
+      m0 = fmaxf(m0, acc[mt][0]);
+      m1 = fmaxf(m1, acc[mt][1]);
+    }
+    if (16 * mt + g + 8 < M) {
+      m0 = fmaxf(m0, acc[mt][2]);
+      m1 = fmaxf(m1, acc[mt][3]);
+    }
+  }
+  m0 = warp_max_xor_g(m0);
+  m1 = warp_max_xor_g(m1);
+  if (g == 0) {
+    const int col = n0 + 2 * t;
+    // a float2 store needs an even element offset (out_off + col); odd NB breaks it
+    const bool even = ((out_off + col) & 1) == 0;
+    if (col + 1 < NB && even) {
+      __stcs(reinterpret_cast<float2*>(out + col), make_float2(m0, m1));
+    } else {
+      if (col < NB) out[col] = m0;
+      if (col + 1 < NB) out[col + 1] = m1;
+    }
+  }
+}
 
 template <int MT>
 __global__ void __launch_bounds__(kScoreThreads) score_kernel(
     const uint16_t* __restrict__ q_draft, const float* __restrict__ summ,
     float* __restrict__ scores, int L, int Hq, int Hkv, int G, int NB, int tpw) {
-  // A fragments, laid out [mt][p][half][lane] so each warp read is contiguous
-  extern __shared__ float4 sQ[];
+  // shared memory: A fragments [mt][p][half][lane], then one ring per warp of
+  // kScoreStages tiles, each [p][lane] float4 (a lane reads back what it copied)
+  extern __shared__ float4 smem4[];
+  float4* sQ = smem4;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
+  float4* ring = smem4 + MT * 8 * 2 * 32 + warp * kScoreStages * 8 * 32;
+  const uint32_t ring_s = smem_u32(ring);
   const int u = blockIdx.y;
   const int b = u / Hkv, h = u - b * Hkv;
   const int M = L * G;
+
+  const int ntiles = (NB + 7) >> 3;
+  const int tile_base = blockIdx.x * kScoreWarps * tpw + warp;
+  const float* base = summ + static_cast<int64_t>(u) * NB * kHeadDim;
+  const int64_t out_off = static_cast<int64_t>(u) * NB;
+  float* out = scores + out_off;
+
+  // copies tile i of this warp into stage i % kScoreStages (one commit group per call)
+  auto issue = [&](int i) {
+    const int tile = tile_base + kScoreWarps * i;
+    if (i < tpw && tile < ntiles) {
+      const int blk = tile * 8 + g;
+      const int st = i % kScoreStages;
+      if (blk < NB) {
+        const float4* src = reinterpret_cast<const float4*>(base + static_cast<int64_t>(blk) * kHeadDim) + t;
+#pragma unroll
+        for (int p = 0; p < 8; ++p)
+          cp_async16(ring_s + static_cast<uint32_t>(((st * 8 + p) * 32 + lane) * 16), src + 4 * p);
+      } else {
+#pragma unroll
+        for (int p = 0; p < 8; ++p) ring[(st * 8 + p) * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int i = 0; i < kScoreStages - 1; ++i) issue(i);
 
   for (int idx = tid; idx < MT * 8 * 2 * 32; idx += kScoreThreads) {
     const int ln = idx & 31, half = (idx >> 5) & 1, p = (idx >> 6) & 7, mt = idx >> 9;
@@ -57,90 +161,39 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(
   }
   __syncthreads();
 
-  const int ntiles = (NB + 7) >> 3;
-  const int tile_base = blockIdx.x * kScoreWarps * tpw;
-  const float* base = summ + static_cast<int64_t>(u) * NB * kHeadDim;
-  float* out = scores + static_cast<int64_t>(u) * NB;
-
 #pragma unroll 1
   for (int i = 0; i < tpw; ++i) {
-    const int tile = tile_base + warp + kScoreWarps * i;
+    const int tile = tile_base + kScoreWarps * i;
     if (tile >= ntiles) break;
-    const int n0 = tile * 8;
-    const int blk = n0 + g;
+    issue(i + kScoreStages - 1);
+    cp_async_wait<kScoreStages - 1>();  // tile i has landed (this lane's copies)
+    const int st = i % kScoreStages;
     float4 v[8];
-    if (blk < NB) {
-      const float4* src = reinterpret_cast<const float4*>(base + static_cast<int64_t>(blk) * kHeadDim) + t;
 #pragma unroll
-      for (int p = 0; p < 8; ++p) v[p] = __ldcs(src + 4 * p);
-    } else {
-#pragma unroll
-      for (int p = 0; p < 8; ++p) v[p] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    float acc[MT][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      const uint32_t hx = to_tf32(v[p].x), hy = to_tf32(v[p].y);
-      const uint32_t hz = to_tf32(v[p].z), hw = to_tf32(v[p].w);
-      const uint32_t lx = to_tf32(v[p].x - __uint_as_float(hx));
-      const uint32_t ly = to_tf32(v[p].y - __uint_as_float(hy));
-      const uint32_t lz = to_tf32(v[p].z - __uint_as_float(hz));
-      const uint32_t lw = to_tf32(v[p].w - __uint_as_float(hw));
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        const float4 qa = sQ[((mt * 8 + p) * 2 + 0) * 32 + lane];
-        const float4 qb = sQ[((mt * 8 + p) * 2 + 1) * 32 + lane];
-        const uint32_t a0 = __float_as_uint(qa.x), a1 = __float_as_uint(qb.x);
-        const uint32_t a2 = __float_as_uint(qa.y), a3 = __float_as_uint(qb.y);
-        const uint32_t c0 = __float_as_uint(qa.z), c1 = __float_as_uint(qb.z);
-        const uint32_t c2 = __float_as_uint(qa.w), c3 = __float_as_uint(qb.w);
-        mma_tf32_1688(acc[mt], a0, a1, a2, a3, hx, hy);  // k-step 2p, hi
-        mma_tf32_1688(acc[mt], a0, a1, a2, a3, lx, ly);  // k-step 2p, lo
-        mma_tf32_1688(acc[mt], c0, c1, c2, c3, hz, hw);  // k-step 2p+1, hi
-        mma_tf32_1688(acc[mt], c0, c1, c2, c3, lz, lw);  // k-step 2p+1, lo
-      }
-    }
-    // max over the valid query rows (rows >= L*G are padding)
-    float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      if (16 * mt + g < M) {
-        m0 = fmaxf(m0, acc[mt][0]);
-        m1 = fmaxf(m1, acc[mt][1]);
-      }
-      if (16 * mt + g + 8 < M) {
-        m0 = fmaxf(m0, acc[mt][2]);
-        m1 = fmaxf(m1, acc[mt][3]);
-      }
-    }
-    m0 = warp_max_xor_g(m0);
-    m1 = warp_max_xor_g(m1);
-    if (g == 0) {
-      const int col = n0 + 2 * t;
-      if (col + 1 < NB) {
-        __stcs(reinterpret_cast<float2*>(out + col), make_float2(m0, m1));
-      } else if (col < NB) {
-        out[col] = m0;
-      }
-    }
+    for (int p = 0; p < 8; ++p) v[p] = ring[(st * 8 + p) * 32 + lane];
+    score_tile<MT>(v, sQ, lane, g, t, M, tile * 8, NB, out_off, out);
   }
+  cp_async_wait<0>();
+}
+
+static size_t score_smem_bytes(int mt) {
+  return sizeof(float4) * (static_cast<size_t>(mt) * 8 * 2 * 32 + kScoreWarps * kScoreStages * 8 * 32);
 }
 
 template <int MT>
 static cudaError_t launch_mt(const Shape& s, const uint16_t* q_draft, const float* summ,
                              float* scores, cudaStream_t st, const DeviceInfo& di) {
+  // one wave: as many CTAs per (request, KV head) as the resident CTA slots allow
   const int ntiles = (s.NB + 7) / 8;
-  const int64_t total_tiles = static_cast<int64_t>(ntiles) * s.units();
-  int per_sm = di.score_ctas_per_sm > 0 ? di.score_ctas_per_sm : 2;
-  const int64_t warps_resident = static_cast<int64_t>(di.sm_count > 0 ? di.sm_count : 148) * per_sm * kScoreWarps;
-  int tpw = static_cast<int>((total_tiles + warps_resident - 1) / warps_resident);
+  const int per_sm = di.score_ctas_per_sm > 0 ? di.score_ctas_per_sm : 2;
+  const int64_t slots = static_cast<int64_t>(di.sm_count > 0 ? di.sm_count : 148) * per_sm;
+  int cpu = static_cast<int>(slots / s.units());
+  if (cpu < 1) cpu = 1;
+  int tpw = (ntiles + kScoreWarps * cpu - 1) / (kScoreWarps * cpu);
   if (tpw < 1) tpw = 1;
   const int ctas_per_unit = (ntiles + kScoreWarps * tpw - 1) / (kScoreWarps * tpw);
   dim3 grid(ctas_per_unit, s.units());
-  const size_t smem = sizeof(float4) * MT * 8 * 2 * 32;
-  score_kernel<MT><<<grid, kScoreThreads, smem, st>>>(q_draft, summ, scores, s.L, s.Hq, s.Hkv,
+  score_kernel<MT><<<grid, kScoreThreads, score_smem_bytes(MT), st>>>(q_draft, summ, scores, s.L, s.Hq, s.Hkv,
                                                       s.G, s.NB, tpw);
   return cudaGetLastError();
 }
@@ -157,10 +210,19 @@ cudaError_t launch_score_blocks(const Shape& s, const uint16_t* q_draft, const f
   }
 }
 
+cudaError_t score_configure() {
+  cudaError_t e = cudaSuccess;
+  e = cudaFuncSetAttribute(score_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)score_smem_bytes(1));
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(score_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)score_smem_bytes(2));
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(score_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)score_smem_bytes(3));
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(score_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)score_smem_bytes(4));
+  return e;
+}
+
 int score_ctas_per_sm() {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, score_kernel<1>, kScoreThreads,
-                                                    sizeof(float4) * 8 * 2 * 32) != cudaSuccess)
+                                                    score_smem_bytes(1)) != cudaSuccess)
     return 2;
   return n > 0 ? n : 1;
 }

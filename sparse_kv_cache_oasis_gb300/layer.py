@@ -115,6 +115,14 @@ class LayerState:
                                     self.fetch_slot, self.evict_block, self.n_fetch, self.n_evict,
                                     stream)
 
+    def predict_fused(self, q_draft, stream=None):
+        """Scoring, then top-K and planning fused in one launch (device clock)."""
+        ob.oasis_score_blocks(self.cfg, q_draft, self.summ, self.scores, stream)
+        ob.oasis_predict_select(self.cfg, self.scores, 0, self.clock, self.topk,
+                                self.slot_of_block, self.block_of_slot, self.last_used,
+                                self.fetch_block, self.fetch_slot, self.evict_block,
+                                self.n_fetch, self.n_evict, stream)
+
     def fetch(self, stream=None):
         ob.oasis_fetch_blocks(self.cfg, self.host_k_dev, self.host_v_dev, self.fetch_block,
                               self.fetch_slot, self.n_fetch, self.pool_k, self.pool_v, stream)

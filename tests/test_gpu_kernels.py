@@ -342,3 +342,41 @@ def test_plan_clocked_equals_plan_with_step():
         for x, y in zip(a + oa, b + obuf):
             assert torch.equal(x, y)
         assert (clock == t + 1).all()
+
+
+@pytest.mark.parametrize("NB,S,K,ratio,sink,local", [
+    (2048, 128, 128, 0.05, 0, 0), (8192, 128, 128, 0.02, 1, 4), (300, 40, 30, 0.5, 2, 2),
+    (5000, 1024, 1000, -1.0, 0, 0), (64, 8, 8, 0.0, 0, 0)])
+def test_predict_select_fused_equals_separate(NB, S, K, ratio, sink, local):
+    rs = np.random.default_rng(NB + K)
+    B, H = 2, 3
+    cfg = dict(batch=B, num_q_heads=H, num_kv_heads=H, head_dim=128, block_size=16, num_blocks=NB,
+               kv_budget_tokens=16 * S, lookahead=1, top_k=K, fetch_ratio=ratio, sink_blocks=sink,
+               local_blocks=local)
+    sob, bos, lu = _random_state(rs, B, H, NB, S, full=(S <= NB))
+    w = max(oracle.fetch_cap(cfg), 1)
+
+    def bufs():
+        st = [torch.from_numpy(x.copy()).cuda() for x in (sob, bos, lu)]
+        out = [torch.full((B, H, w), -9, dtype=torch.int32, device="cuda") for _ in range(3)] + \
+              [torch.full((B, H), -9, dtype=torch.int32, device="cuda") for _ in range(2)]
+        return st, out, torch.full((B, H, K), -9, dtype=torch.int32, device="cuda")
+
+    a_st, a_out, a_topk = bufs()
+    b_st, b_out, b_topk = bufs()
+    clock = torch.full((B, H), 3, dtype=torch.int32, device="cuda")
+    for t in range(3, 7):
+        scores = torch.from_numpy(rs.standard_normal((B, H, NB)).astype(np.float32)).cuda()
+        ob.oasis_select_topk(cfg, scores, a_topk)
+        ob.oasis_plan_fetch(cfg, a_topk, t, *a_st, *a_out)
+        if t % 2:
+            ob.oasis_predict_select(cfg, scores, 0, clock, b_topk, *b_st, *b_out)
+        else:
+            ob.oasis_predict_select(cfg, scores, t, None, b_topk, *b_st, *b_out)
+            clock += 1
+        torch.cuda.synchronize()
+        assert torch.equal(a_topk, b_topk)
+        for x, y in zip(a_st + a_out, b_st + b_out):
+            assert torch.equal(x, y)
+        # and the oracle agrees on the plan
+    assert ob.oasis_device_errors() == 0
