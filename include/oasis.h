@@ -206,6 +206,30 @@ oasis_status_t oasis_sparse_decode_attn(const oasis_config_t* cfg, const uint16_
 /* Scratch bytes oasis_sparse_decode_attn needs for `cfg` (0 on invalid cfg). */
 size_t oasis_attn_workspace_bytes(const oasis_config_t* cfg);
 
+/* oasis_sparse_decode_attn for callers that cannot allocate device memory --
+ * for example code running inside another framework's memory pool or
+ * allocator hooks, under a device-memory quota, or on a latency-critical path
+ * where a cudaMalloc (which may synchronize) is not acceptable.  The method's
+ * pages have no counterpart: this is a deployment convenience.
+ * Same arguments and result as oasis_sparse_decode_attn, without the
+ * workspace: the scratch is a fixed 8 MiB array in device memory that every
+ * GPU that loads this library holds until the process exits.  The caller
+ * still owns q, the pools, block_of_slot, ctx_len and out.  Nothing is
+ * allocated: no cudaMalloc, no cudaFree, no allocating library call.
+ * Configurations needing more scratch than 8 MiB (see
+ * oasis_attn_workspace_bytes) return OASIS_ERR_UNSUPPORTED and launch
+ * nothing.  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  Every call clears the array's arrival counters on
+ * `stream` before its kernel; the rest of the array keeps what the last call
+ * left.  All calls on a device share the one array, so calls that overlap on
+ * the GPU (different streams without ordering) race and give wrong results. */
+oasis_status_t oasis_sparse_decode_attn_static(const oasis_config_t* cfg, const uint16_t* q,
+                                               const uint16_t* pool_k, const uint16_t* pool_v,
+                                               const int32_t* block_of_slot,
+                                               const int32_t* ctx_len, float scale,
+                                               uint16_t* out, void* stream);
+
 /* Pins and maps `bytes` of existing host memory at `host` (cudaHostRegister,
  * mapped) and returns in *dev_ptr the address kernels use to read it: the
  * form oasis_fetch_blocks expects for host_k / host_v.  Not for the per-step

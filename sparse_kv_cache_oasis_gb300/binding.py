@@ -62,6 +62,8 @@ _SIGS = {
     "oasis_sparse_decode_attn": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P, _P, _P, C.c_float,
                                            _P, _P, C.c_size_t, _P]),
     "oasis_attn_workspace_bytes": (C.c_size_t, [C.POINTER(OasisConfig)]),
+    "oasis_sparse_decode_attn_static": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P, _P, _P,
+                                                  C.c_float, _P, _P]),
     "oasis_host_register": (C.c_int, [_P, C.c_size_t, C.POINTER(C.c_void_p)]),
     "oasis_host_unregister": (C.c_int, [_P]),
     "oasis_device_errors": (C.c_int, [C.POINTER(C.c_uint32), C.c_int32]),
@@ -272,6 +274,21 @@ def oasis_sparse_decode_attn(cfg, q, pool_k, pool_v, block_of_slot, ctx_len, sca
         _ptr(pool_v, torch.bfloat16, (B, H, S, bs, D), "pool_v"),
         _ptr(block_of_slot, torch.int32, (B, H, S), "block_of_slot"), cl, float(scale),
         _ptr(out, torch.bfloat16, (B, Hq, D), "out"), ws, nbytes, _stream(stream)))
+
+
+def oasis_sparse_decode_attn_static(cfg, q, pool_k, pool_v, block_of_slot, ctx_len, scale, out,
+                                    stream=None) -> None:
+    """oasis_sparse_decode_attn without a workspace argument: the library's
+    fixed device scratch is used instead, so the call allocates nothing."""
+    c = OasisConfig.make(cfg)
+    B, H, Hq, NB, bs, D, S = _dims(c)
+    cl = None if ctx_len is None else _ptr(ctx_len, torch.int32, (B,), "ctx_len")
+    _check("oasis_sparse_decode_attn_static", lib().oasis_sparse_decode_attn_static(
+        C.byref(c), _ptr(q, torch.bfloat16, (B, Hq, D), "q"),
+        _ptr(pool_k, torch.bfloat16, (B, H, S, bs, D), "pool_k"),
+        _ptr(pool_v, torch.bfloat16, (B, H, S, bs, D), "pool_v"),
+        _ptr(block_of_slot, torch.int32, (B, H, S), "block_of_slot"), cl, float(scale),
+        _ptr(out, torch.bfloat16, (B, Hq, D), "out"), _stream(stream)))
 
 
 def oasis_host_register(tensor: torch.Tensor) -> int:

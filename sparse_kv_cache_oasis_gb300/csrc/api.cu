@@ -146,6 +146,27 @@ oasis_status_t encode_pool(CUtensorMap* tm, const void* pool, const Shape& s) {
   return r == CUDA_SUCCESS ? OASIS_OK : OASIS_ERR_INVALID_ARG;
 }
 
+// Scratch of oasis_sparse_decode_attn_static: a fixed array in device memory
+// that exists on every GPU this library is loaded on, so that call needs no
+// allocation.  In host code the name is only a stand-in; the device address is
+// looked up once per device with cudaGetSymbolAddress.
+constexpr size_t kStaticAttnScratchBytes = 8u << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_static_attn_scratch[kStaticAttnScratchBytes];
+void* g_static_scratch_addr[kMaxDevices];
+
+oasis_status_t static_attn_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return OASIS_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_static_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_attn_scratch) != cudaSuccess || !p) return OASIS_ERR_CUDA;
+    g_static_scratch_addr[dev] = p;
+  }
+  *out = g_static_scratch_addr[dev];
+  return OASIS_OK;
+}
+
 }  // namespace
 }  // namespace oasis
 
@@ -324,6 +345,37 @@ oasis_status_t oasis_host_register(void* host, size_t bytes, void** dev_ptr) {
 oasis_status_t oasis_host_unregister(void* host) {
   if (!host) return OASIS_ERR_INVALID_ARG;
   return from_cuda(cudaHostUnregister(host));
+}
+
+oasis_status_t oasis_sparse_decode_attn_static(const oasis_config_t* cfg, const uint16_t* q,
+                                               const uint16_t* pool_k, const uint16_t* pool_v,
+                                               const int32_t* block_of_slot,
+                                               const int32_t* ctx_len, float scale,
+                                               uint16_t* out, void* stream) {
+  Shape s;
+  oasis_status_t st = make_shape(cfg, &s);
+  if (st != OASIS_OK) return st;
+  if (s.G > kMaxAttnGroup) return OASIS_ERR_UNSUPPORTED;
+  if (attn_workspace_bytes(s) > kStaticAttnScratchBytes) return OASIS_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return OASIS_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(pool_k, 16) || !aligned(pool_v, 16) || !aligned(out, 16) ||
+      !aligned(block_of_slot, 4))
+    return OASIS_ERR_INVALID_ARG;
+  if (ctx_len && !aligned(ctx_len, 4)) return OASIS_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != OASIS_OK) return st;
+  void* scratch = nullptr;
+  if ((st = static_attn_scratch(&scratch)) != OASIS_OK) return st;
+  CUtensorMap tk, tv;
+  if ((st = encode_pool(&tk, pool_k, s)) != OASIS_OK) return st;
+  if ((st = encode_pool(&tv, pool_v, s)) != OASIS_OK) return st;
+  // the array keeps whatever the previous call left; the arrival counters must start at zero
+  const size_t cnt = attn_counter_bytes(s);
+  if (cnt && cudaMemsetAsync(static_cast<unsigned char*>(scratch) + attn_counter_offset(s), 0, cnt,
+                             static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return OASIS_ERR_CUDA;
+  return from_cuda(launch_sparse_decode_attn(s, q, tk, tv, block_of_slot, ctx_len, scale, out,
+                                             scratch, static_cast<cudaStream_t>(stream), di));
 }
 
 oasis_status_t oasis_device_errors(uint32_t* flags, int32_t clear) {

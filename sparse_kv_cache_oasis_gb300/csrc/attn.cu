@@ -52,6 +52,17 @@ size_t attn_workspace_bytes(const Shape& s) {
   return ((part + 255) / 256) * 256 + ((cnt + 255) / 256) * 256;
 }
 
+// Where the per-unit arrival counters sit in the workspace, and their size
+// (none when a unit fits one CTA); they must be zero before a call.
+size_t attn_counter_offset(const Shape& s) {
+  const size_t part = static_cast<size_t>(s.units()) * ctas_per_unit_of(s.S) * kMaxGroup *
+                      kPartStride * sizeof(float);
+  return ((part + 255) / 256) * 256;
+}
+size_t attn_counter_bytes(const Shape& s) {
+  return ctas_per_unit_of(s.S) > 1 ? static_cast<size_t>(s.units()) * sizeof(int) : 0;
+}
+
 // byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a 128B-swizzled 16x64 bf16 box
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));

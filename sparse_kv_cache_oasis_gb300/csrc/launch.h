@@ -50,6 +50,8 @@ cudaError_t launch_fetch_blocks(const Shape& s, const uint16_t* host_k, const ui
 
 // Attention: the pools are read by TMA through these two tensor maps.
 size_t attn_workspace_bytes(const Shape& s);
+size_t attn_counter_offset(const Shape& s);  // arrival counters inside the workspace
+size_t attn_counter_bytes(const Shape& s);
 cudaError_t attn_configure(int device);  // one-time function attributes
 int attn_ctas_per_sm();
 cudaError_t launch_sparse_decode_attn(const Shape& s, const uint16_t* q,
