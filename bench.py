@@ -14,8 +14,10 @@ independent copies of the layer (distinct seeds) are cycled step after step,
 as consecutive layers of a model would be: the working set touched between
 two visits of the same copy (4 x 134 MB) is larger than L2, and the transfer
 of one layer overlaps the next layer's compute (copy stream), as in Fig. 8.
-Each layer copy replays a CUDA graph per query set; the LRU step lives in
-device memory (oasis_plan_fetch_clocked), so replays advance it.
+Each step replays a CUDA graph: attention of copy s beside scoring of copy
+s-1, top-K + plan of copy s-2 and the transfer of copy s-3 (a software
+pipeline over layers); the LRU step lives in device memory, so replays
+advance it.
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the
 same workload instead.
@@ -304,7 +306,8 @@ def gpu_arm(args):
     torch.cuda.synchronize()
 
     compute = torch.cuda.Stream(device=dev)
-    pred = torch.cuda.Stream(device=dev)
+    score_st = torch.cuda.Stream(device=dev)
+    select_st = torch.cuda.Stream(device=dev)
     copy = torch.cuda.Stream(device=dev, priority=-1)
     out_host = [torch.empty_like(L.out, device="cpu").pin_memory() for L in layers]
     q_in = [torch.empty_like(q_dev[i][0]) for i in range(n_inst)]
@@ -313,32 +316,41 @@ def gpu_arm(args):
     def qset(s):
         return s % n_inst, (s // n_inst) % QUERY_SETS
 
-    def enqueue(s, s_lo, s_hi, host_io: bool):
-        """Graph body of step s (a software pipeline over the layer copies, as
-        in Fig. 8): attention of step s on `compute`; beside it, prediction
-        (scoring, top-K, plan) of step s-1 on `pred` and the transfer of step
-        s-2 on `copy`.  Only steps in [s_lo, s_hi) are issued, so the first and
-        last graphs of a run fill and drain the pipeline.  Copy s % 4 is
-        touched by nothing else inside the graph: step s-1 and s-2 use other
-        copies, and their previous transfer/plan finished in earlier graphs."""
+    def enqueue(s, active, host_io: bool):
+        """Graph body of step s, a software pipeline over the layer copies as in
+        Fig. 8 (each layer's prediction and transfer run in the background of
+        the following layers): attention of step s on `compute`, and beside it
+        scoring of step s-1, top-K + plan of step s-2 and the transfer of step
+        s-3, each on its own stream.  `active` = which of the four run (the
+        first and last graphs of a run fill and drain the pipeline).  The four
+        steps use four different layer copies, and each one's inputs were
+        produced by an earlier graph."""
         fork = torch.cuda.Event()
         fork.record(compute)
         joins = []
-        if s_lo <= s - 1 < s_hi:
+
+        def branch(stream, fn):
+            stream.wait_event(fork)
+            fn(stream)
+            e = torch.cuda.Event()
+            e.record(stream)
+            joins.append(e)
+
+        if "score" in active:
             i1, qi1 = qset(s - 1)
-            pred.wait_event(fork)
             qd = qd_in[i1] if host_io else qd_dev[i1][qi1]
-            layers[i1].predict_fused(qd, pred)
-            e = torch.cuda.Event()
-            e.record(pred)
-            joins.append(e)
-        if s_lo <= s - 2 < s_hi:
-            copy.wait_event(fork)
-            layers[(s - 2) % n_inst].fetch(copy)
-            e = torch.cuda.Event()
-            e.record(copy)
-            joins.append(e)
-        if s_lo <= s < s_hi:
+            L1 = layers[i1]
+            branch(score_st, lambda st: ob.oasis_score_blocks(L1.cfg, qd, L1.summ, L1.scores, st))
+        if "select" in active:
+            L2 = layers[(s - 2) % n_inst]
+            branch(select_st, lambda st: ob.oasis_predict_select(
+                L2.cfg, L2.scores, 0, L2.clock, L2.topk, L2.slot_of_block, L2.block_of_slot,
+                L2.last_used, L2.fetch_block, L2.fetch_slot, L2.evict_block, L2.n_fetch,
+                L2.n_evict, st))
+        if "fetch" in active:
+            L3 = layers[(s - 3) % n_inst]
+            branch(copy, lambda st: L3.fetch(st))
+        if "attn" in active:
             i, qi = qset(s)
             L = layers[i]
             if host_io:
@@ -353,39 +365,44 @@ def gpu_arm(args):
         for e in joins:
             compute.wait_event(e)
 
+    def active_of(s, s0, n):
+        parts = []
+        for name, lag in (("attn", 0), ("score", 1), ("select", 2), ("fetch", 3)):
+            if s0 <= s - lag < s0 + n:
+                parts.append(name)
+        return frozenset(parts)
+
     # ---- warm the library (first calls set up per-device state)
     with torch.cuda.stream(compute):
-        for s_ in range(2 * n_inst + 2):
-            enqueue(s_, 0, 2 * n_inst, host_io=False)
+        for s_ in range(2 * n_inst + 3):
+            enqueue(s_, active_of(s_, 0, 2 * n_inst), host_io=False)
     torch.cuda.synchronize()
     period = n_inst * QUERY_SETS
     graphs = {}
 
-    def graph_for(s, a, b, host_io):
-        """Graph of step s issuing only the steps in [s + a, s + b)."""
-        key = (s % period, a, b, host_io)
+    def graph_for(s, active, host_io):
+        key = (s % period, active, host_io)
         if key not in graphs:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=compute):
-                enqueue(s, s + a, s + b, host_io)
+                enqueue(s, active, host_io)
             graphs[key] = g
         return graphs[key]
 
     def run_steps(s0, n, host_io=False):
-        """Exactly the work of layer-steps s0..s0+n-1: n + 2 graph replays
-        (the pipeline fills in the first two and drains in the last two)."""
+        """Exactly the work of layer-steps s0..s0+n-1: n + 3 graph replays
+        (the pipeline fills in the first three and drains in the last three)."""
         with torch.cuda.stream(compute):
-            for s in range(s0, s0 + n + 2):
-                a, b = max(-2, s0 - s), min(1, s0 + n - s)
-                graph_for(s, a, b, host_io).replay()
+            for s in range(s0, s0 + n + 3):
+                graph_for(s, active_of(s, s0, n), host_io).replay()
 
-    # capture every graph the runs below need, outside the timed regions
-    variants = [(-2, -1), (-2, 0), (-2, 1), (-1, 0), (-1, 1), (0, 1)]
+    # capture every graph the long runs below need, outside the timed regions
+    long_masks = {active_of(s, 100, 50) for s in range(100, 153)}
     for s in range(period):
-        for a, b in variants:
-            graph_for(s, a, b, False)
+        for m in long_masks:
+            graph_for(s, m, False)
             if not args.no_e2e:
-                graph_for(s, a, b, True)
+                graph_for(s, m, True)
     torch.cuda.synchronize()
 
     if args.profile_steps:
@@ -540,7 +557,7 @@ def gpu_arm(args):
                 "layers": 1, "layer_copies_cycled": n_inst, "parallelism": f"replicas x{world}",
                 "l2": f"inputs larger than L2: {n_inst} layer copies of {by['hbm'] / 1e6:.0f} MB cycled",
                 "tok_s_if_32_layers": value / 32,
-                "graphs": "one CUDA graph per (layer copy, query set); LRU step in device memory"},
+                "graphs": "per-step CUDA graph: attn(s) | score(s-1) | select(s-2) | transfer(s-3); LRU step in device memory"},
             "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
                          "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",

@@ -33,8 +33,6 @@
 namespace oasis {
 
 constexpr int kPredThreads = 1024;
-constexpr int kMaxK = 1024;
-constexpr int kMaxNBWords = 32768 / 32;
 
 __device__ __forceinline__ uint32_t orderable(float f) {
   uint32_t b = __float_as_uint(f);
@@ -42,31 +40,75 @@ __device__ __forceinline__ uint32_t orderable(float f) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// Shared-memory views, carved from dynamic shared memory sized to the shape
+// (top-K and plan scratch share one region: the plan starts after the top-K
+// list is final).
 struct TopkSmem {
-  int hist[256];
-  int digit, greater, equal, count;
-  int scan[33];
-  unsigned long long keys[kMaxK];
+  unsigned long long* keys;  // [K]
+  int* hist;                 // [256]
+  int* digit;
+  int* greater;
+  int* equal;
+  int* count;
+  int* scan;                 // [33]
 };
 
 struct PlanSmem {
-  unsigned long long lru_key[kMaxK];   // per slot: candidate key or ~0
-  int bos[kMaxK];                      // block of slot (updated in place)
-  int lu[kMaxK];                       // last used (updated in place)
-  unsigned int seen[kMaxNBWords];      // bitmap of predicted ids
-  int fetch[kMaxK];                    // fetched blocks, priority order
-  int free_slot[kMaxK];                // free slots, ascending
-  int victim[kMaxK];                   // victim blocks, LRU order
-  int inp[kMaxK];                      // slot holds a predicted block
-  int scan[33];
-  int bad;
+  unsigned long long* lru_key;  // [S] per slot: candidate key or ~0
+  int* bos;                     // [S] block of slot (updated in place)
+  int* lu;                      // [S] last used (updated in place)
+  int* inp;                     // [S] slot holds a predicted block
+  unsigned int* seen;           // [ceil(NB/32)] bitmap of predicted ids
+  int* fetch;                   // [capw] fetched blocks, priority order
+  int* free_slot;               // [capw] free slots, ascending
+  int* victim;                  // [capw] victim blocks, LRU order
+  int* scan;                    // [33]
+  int* bad;
+};
+
+struct PredLayout {
+  int K, S, NB, capw;
+  __host__ __device__ size_t list_bytes() const { return ((static_cast<size_t>(K) * 4 + 7) / 8) * 8; }
+  __host__ __device__ size_t topk_bytes() const { return static_cast<size_t>(K) * 8 + (256 + 4 + 33) * 4; }
+  __host__ __device__ size_t plan_bytes() const {
+    return static_cast<size_t>(S) * 8 + static_cast<size_t>(S) * 12 + static_cast<size_t>((NB + 31) / 32) * 4 +
+           static_cast<size_t>(capw) * 12 + (33 + 1) * 4;
+  }
+  __host__ __device__ size_t bytes() const {
+    const size_t t = topk_bytes(), q = plan_bytes();
+    return list_bytes() + (t > q ? t : q);
+  }
+  __device__ void carve(unsigned char* base, int** list, TopkSmem* tk, PlanSmem* pl) const {
+    *list = reinterpret_cast<int*>(base);
+    unsigned char* r = base + list_bytes();
+    tk->keys = reinterpret_cast<unsigned long long*>(r);
+    int* ti = reinterpret_cast<int*>(r + static_cast<size_t>(K) * 8);
+    tk->hist = ti;
+    tk->digit = ti + 256;
+    tk->greater = ti + 257;
+    tk->equal = ti + 258;
+    tk->count = ti + 259;
+    tk->scan = ti + 260;
+    pl->lru_key = reinterpret_cast<unsigned long long*>(r);
+    int* pi = reinterpret_cast<int*>(r + static_cast<size_t>(S) * 8);
+    pl->bos = pi;
+    pl->lu = pi + S;
+    pl->inp = pi + 2 * S;
+    pl->seen = reinterpret_cast<unsigned int*>(pi + 3 * S);
+    int* after = pi + 3 * S + (NB + 31) / 32;
+    pl->fetch = after;
+    pl->free_slot = after + capw;
+    pl->victim = after + 2 * capw;
+    pl->scan = after + 3 * capw;
+    pl->bad = after + 3 * capw + 33;
+  }
 };
 
 // Writes the unit's top-K list (priority order) to `out_smem` (K ints) and,
 // if out_global is not null, to global memory.  All threads must call it.
 template <int ITEMS>
 __device__ void topk_unit(const float* __restrict__ sc, int NB, int K, int sink, int local,
-                          int* out_smem, int32_t* __restrict__ out_global, TopkSmem& sm) {
+                          int* out_smem, int32_t* __restrict__ out_global, const TopkSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T = blockDim.x;
   const int a = sink < NB ? sink : NB;
@@ -123,19 +165,19 @@ __device__ void topk_unit(const float* __restrict__ sc, int NB, int K, int sink,
 #pragma unroll
       for (int k = 7; k >= 0; --k) {
         if (running < remaining && running + c[k] >= remaining) {
-          sm.digit = lane * 8 + k;
-          sm.greater = running;
-          sm.equal = c[k];
+          *sm.digit = lane * 8 + k;
+          *sm.greater = running;
+          *sm.equal = c[k];
         }
         running += c[k];
       }
     }
     __syncthreads();
-    prefix |= static_cast<uint32_t>(sm.digit) << shift;
+    prefix |= static_cast<uint32_t>(*sm.digit) << shift;
     mask |= 255u << shift;
-    remaining -= sm.greater;
+    remaining -= *sm.greater;
   }
-  const int n_equal = sm.equal;
+  const int n_equal = *sm.equal;
   int eq_rank[ITEMS];
 #pragma unroll
   for (int it = 0; it < ITEMS; ++it) eq_rank[it] = 0;
@@ -149,7 +191,7 @@ __device__ void topk_unit(const float* __restrict__ sc, int NB, int K, int sink,
       base += tot;
     }
   }
-  if (tid == 0) sm.count = 0;
+  if (tid == 0) *sm.count = 0;
   __syncthreads();
 #pragma unroll
   for (int it = 0; it < ITEMS; ++it) {
@@ -158,11 +200,11 @@ __device__ void topk_unit(const float* __restrict__ sc, int NB, int K, int sink,
         valid[it] && (key[it] > prefix || (key[it] == prefix && eq_rank[it] < remaining));
     const unsigned bal = __ballot_sync(0xffffffffu, sel);
     int base = 0;
-    if (lane == 0 && bal) base = atomicAdd(&sm.count, __popc(bal));
+    if (lane == 0 && bal) base = atomicAdd(sm.count, __popc(bal));
     base = __shfl_sync(0xffffffffu, base, 0);
     if (sel) {
       const int pos = base + __popc(bal & ((1u << lane) - 1u));
-      if (pos < kMaxK)
+      if (pos < K)
         sm.keys[pos] = (static_cast<unsigned long long>(key[it]) << 32) |
                        static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(j));
     }
@@ -215,9 +257,9 @@ __device__ void plan_unit(const int* P, const SlotView v, int32_t step, int32_t*
                           int32_t* __restrict__ lu, int32_t* __restrict__ fetch_block,
                           int32_t* __restrict__ fetch_slot, int32_t* __restrict__ evict_block,
                           int32_t* __restrict__ n_fetch_u, int32_t* __restrict__ n_evict_u,
-                          int NB, int S, int K, int cap, int capw, uint32_t* err, PlanSmem& sm) {
+                          int NB, int S, int K, int cap, int capw, uint32_t* err, const PlanSmem& sm) {
   const int tid = threadIdx.x, T = blockDim.x;
-  if (tid == 0) sm.bad = 0;
+  if (tid == 0) *sm.bad = 0;
   for (int w = tid; w < (NB + 31) / 32; w += T) sm.seen[w] = 0u;
   if (tid < S) sm.inp[tid] = 0;
   __syncthreads();
@@ -226,20 +268,20 @@ __device__ void plan_unit(const int* P, const SlotView v, int32_t step, int32_t*
   if (tid < K) {
     p = P[tid];
     if (p < 0 || p >= NB) {
-      atomicOr(&sm.bad, OASIS_DEVERR_TOPK_IDS);
+      atomicOr(sm.bad, OASIS_DEVERR_TOPK_IDS);
     } else {
       const unsigned bit = 1u << (p & 31);
-      if (atomicOr(&sm.seen[p >> 5], bit) & bit) atomicOr(&sm.bad, OASIS_DEVERR_TOPK_IDS);
+      if (atomicOr(&sm.seen[p >> 5], bit) & bit) atomicOr(sm.bad, OASIS_DEVERR_TOPK_IDS);
       sp = sob[p];
     }
   }
   if (tid < S && (v.bos >= NB || (v.bos >= 0 && v.chk != tid)))
-    atomicOr(&sm.bad, OASIS_DEVERR_PLAN_STATE);
+    atomicOr(sm.bad, OASIS_DEVERR_PLAN_STATE);
   if (tid < S) sm.bos[tid] = v.bos;
   __syncthreads();
-  if (tid < K && sp >= 0 && (sp >= S || sm.bos[sp] != p)) atomicOr(&sm.bad, OASIS_DEVERR_PLAN_STATE);
+  if (tid < K && sp >= 0 && (sp >= S || sm.bos[sp] != p)) atomicOr(sm.bad, OASIS_DEVERR_PLAN_STATE);
   __syncthreads();
-  const int bad = sm.bad;
+  const int bad = *sm.bad;
   if (bad) {
     if (tid == 0) {
       set_error(err, static_cast<uint32_t>(bad));
@@ -345,11 +387,15 @@ __device__ void plan_unit(const int* P, const SlotView v, int32_t step, int32_t*
 template <int ITEMS>
 __global__ void __launch_bounds__(kPredThreads) topk_kernel(const float* __restrict__ scores,
                                                             int32_t* __restrict__ topk_ids,
-                                                            int NB, int K, int sink, int local) {
-  __shared__ TopkSmem sm;
-  __shared__ int sP[kMaxK];
+                                                            int NB, int K, int sink, int local,
+                                                            PredLayout lay) {
+  extern __shared__ __align__(16) unsigned char pred_smem[];
+  int* sP;
+  TopkSmem tk;
+  PlanSmem pl;
+  lay.carve(pred_smem, &sP, &tk, &pl);
   const int64_t u = blockIdx.x;
-  topk_unit<ITEMS>(scores + u * NB, NB, K, sink, local, sP, topk_ids + u * K, sm);
+  topk_unit<ITEMS>(scores + u * NB, NB, K, sink, local, sP, topk_ids + u * K, tk);
 }
 
 __global__ void __launch_bounds__(kPredThreads) plan_kernel(
@@ -358,9 +404,12 @@ __global__ void __launch_bounds__(kPredThreads) plan_kernel(
     int32_t* __restrict__ last_used, int32_t* __restrict__ fetch_block,
     int32_t* __restrict__ fetch_slot, int32_t* __restrict__ evict_block,
     int32_t* __restrict__ n_fetch, int32_t* __restrict__ n_evict, int NB, int S, int K, int cap,
-    int capw, uint32_t* err) {
-  __shared__ PlanSmem sm;
-  __shared__ int sP[kMaxK];
+    int capw, uint32_t* err, PredLayout lay) {
+  extern __shared__ __align__(16) unsigned char pred_smem[];
+  int* sP;
+  TopkSmem tk;
+  PlanSmem pl;
+  lay.carve(pred_smem, &sP, &tk, &pl);
   const int64_t u = blockIdx.x;
   const int32_t st = clock ? clock[u] : step;
   int32_t* sob = slot_of_block + u * NB;
@@ -369,7 +418,7 @@ __global__ void __launch_bounds__(kPredThreads) plan_kernel(
   __syncthreads();
   plan_unit(sP, v, st, clock ? clock + u : nullptr, sob, block_of_slot + u * S, last_used + u * S,
             fetch_block + u * capw, fetch_slot + u * capw, evict_block + u * capw, n_fetch + u,
-            n_evict + u, NB, S, K, cap, capw, err, sm);
+            n_evict + u, NB, S, K, cap, capw, err, pl);
 }
 
 // Top-K and plan of one unit in one CTA; the map loads overlap the selection.
@@ -381,45 +430,63 @@ __global__ void __launch_bounds__(kPredThreads) topk_plan_kernel(
     int32_t* __restrict__ fetch_block, int32_t* __restrict__ fetch_slot,
     int32_t* __restrict__ evict_block, int32_t* __restrict__ n_fetch,
     int32_t* __restrict__ n_evict, int NB, int S, int K, int cap, int capw, int sink, int local,
-    uint32_t* err) {
-  __shared__ union {
-    TopkSmem topk;
-    PlanSmem plan;
-  } sm;
-  __shared__ int sP[kMaxK];
+    uint32_t* err, PredLayout lay) {
+  extern __shared__ __align__(16) unsigned char pred_smem[];
+  int* sP;
+  TopkSmem tk;
+  PlanSmem pl;
+  lay.carve(pred_smem, &sP, &tk, &pl);
   const int64_t u = blockIdx.x;
   const int32_t st = clock ? clock[u] : step;
   int32_t* sob = slot_of_block + u * NB;
   const SlotView v = load_slot_view(sob, block_of_slot + u * S, last_used + u * S, S, NB);
-  topk_unit<ITEMS>(scores + u * NB, NB, K, sink, local, sP, topk_ids + u * K, sm.topk);
+  topk_unit<ITEMS>(scores + u * NB, NB, K, sink, local, sP, topk_ids + u * K, tk);
   plan_unit(sP, v, st, clock ? clock + u : nullptr, sob, block_of_slot + u * S, last_used + u * S,
             fetch_block + u * capw, fetch_slot + u * capw, evict_block + u * capw, n_fetch + u,
-            n_evict + u, NB, S, K, cap, capw, err, sm.plan);
+            n_evict + u, NB, S, K, cap, capw, err, pl);
 }
 
-static int threads_for(int need) {
-  int t = ((need + 31) / 32) * 32;
-  if (t < 128) t = 128;
-  return t > kPredThreads ? kPredThreads : t;
+// Threads per CTA: 256 unless the slots, the list or the scores (at most 32
+// per thread in registers, 16 where possible) need more.
+static int pred_threads(int need, int NB) {
+  int t = 256;
+  while (t < kPredThreads && (t < need || (NB + t - 1) / t > 16)) t *= 2;
+  return t;
 }
 
-template <int ITEMS>
-static cudaError_t launch_topk_items(const Shape& s, const float* scores, int32_t* topk_ids,
-                                     cudaStream_t st) {
-  topk_kernel<ITEMS><<<s.units(), kPredThreads, 0, st>>>(scores, topk_ids, s.NB, s.K, s.sink, s.local);
-  return cudaGetLastError();
+static PredLayout pred_layout(const Shape& s) {
+  PredLayout lay;
+  lay.K = s.K;
+  lay.S = s.S;
+  lay.NB = s.NB;
+  lay.capw = s.cap > 0 ? s.cap : 1;
+  return lay;
 }
+
+#define OASIS_ITEMS_SWITCH(items, CALL) \
+  do {                                  \
+    if ((items) <= 1) CALL(1);          \
+    if ((items) <= 2) CALL(2);          \
+    if ((items) <= 4) CALL(4);          \
+    if ((items) <= 8) CALL(8);          \
+    if ((items) <= 16) CALL(16);        \
+    if ((items) <= 32) CALL(32);        \
+    return cudaErrorInvalidValue;       \
+  } while (0)
 
 cudaError_t launch_select_topk(const Shape& s, const float* scores, int32_t* topk_ids,
                                cudaStream_t st, const DeviceInfo&) {
-  const int items = (s.NB + kPredThreads - 1) / kPredThreads;
-  if (items <= 1) return launch_topk_items<1>(s, scores, topk_ids, st);
-  if (items <= 2) return launch_topk_items<2>(s, scores, topk_ids, st);
-  if (items <= 4) return launch_topk_items<4>(s, scores, topk_ids, st);
-  if (items <= 8) return launch_topk_items<8>(s, scores, topk_ids, st);
-  if (items <= 16) return launch_topk_items<16>(s, scores, topk_ids, st);
-  if (items <= 32) return launch_topk_items<32>(s, scores, topk_ids, st);
-  return cudaErrorInvalidValue;  // rejected by validation (NB <= 32768)
+  const int T = pred_threads(s.K, s.NB);
+  const int items = (s.NB + T - 1) / T;
+  const PredLayout lay = pred_layout(s);
+#define OASIS_TOPK(N)                                                                              \
+  {                                                                                                \
+    topk_kernel<N><<<s.units(), T, lay.bytes(), st>>>(scores, topk_ids, s.NB, s.K, s.sink, s.local, \
+                                                      lay);                                        \
+    return cudaGetLastError();                                                                     \
+  }
+  OASIS_ITEMS_SWITCH(items, OASIS_TOPK);
+#undef OASIS_TOPK
 }
 
 cudaError_t launch_plan_fetch(const Shape& s, const int32_t* topk_ids, int32_t step,
@@ -428,21 +495,11 @@ cudaError_t launch_plan_fetch(const Shape& s, const int32_t* topk_ids, int32_t s
                               int32_t* evict_block, int32_t* n_fetch, int32_t* n_evict,
                               cudaStream_t st, const DeviceInfo& di) {
   const int capw = s.cap > 0 ? s.cap : 1;
-  plan_kernel<<<s.units(), threads_for(s.S > s.K ? s.S : s.K), 0, st>>>(
+  const PredLayout lay = pred_layout(s);
+  const int need = s.S > s.K ? s.S : s.K;
+  plan_kernel<<<s.units(), pred_threads(need, 0), lay.bytes(), st>>>(
       topk_ids, step, clock, slot_of_block, block_of_slot, last_used, fetch_block, fetch_slot,
-      evict_block, n_fetch, n_evict, s.NB, s.S, s.K, s.cap, capw, di.err);
-  return cudaGetLastError();
-}
-
-template <int ITEMS>
-static cudaError_t launch_tp_items(const Shape& s, const float* scores, int32_t* topk_ids,
-                                   int32_t step, int32_t* clock, int32_t* sob, int32_t* bos,
-                                   int32_t* lu, int32_t* fb, int32_t* fs, int32_t* eb,
-                                   int32_t* nf, int32_t* ne, cudaStream_t st, uint32_t* err) {
-  const int capw = s.cap > 0 ? s.cap : 1;
-  topk_plan_kernel<ITEMS><<<s.units(), kPredThreads, 0, st>>>(
-      scores, topk_ids, step, clock, sob, bos, lu, fb, fs, eb, nf, ne, s.NB, s.S, s.K, s.cap,
-      capw, s.sink, s.local, err);
+      evict_block, n_fetch, n_evict, s.NB, s.S, s.K, s.cap, capw, di.err, lay);
   return cudaGetLastError();
 }
 
@@ -452,19 +509,21 @@ cudaError_t launch_select_and_plan(const Shape& s, const float* scores, int32_t*
                                    int32_t* fetch_block, int32_t* fetch_slot,
                                    int32_t* evict_block, int32_t* n_fetch, int32_t* n_evict,
                                    cudaStream_t st, const DeviceInfo& di) {
-  const int items = (s.NB + kPredThreads - 1) / kPredThreads;
-#define OASIS_TP(N)                                                                           \
-  return launch_tp_items<N>(s, scores, topk_ids, step, clock, slot_of_block, block_of_slot,    \
-                            last_used, fetch_block, fetch_slot, evict_block, n_fetch, n_evict, \
-                            st, di.err)
-  if (items <= 1) OASIS_TP(1);
-  if (items <= 2) OASIS_TP(2);
-  if (items <= 4) OASIS_TP(4);
-  if (items <= 8) OASIS_TP(8);
-  if (items <= 16) OASIS_TP(16);
-  if (items <= 32) OASIS_TP(32);
+  const int capw = s.cap > 0 ? s.cap : 1;
+  const int need = s.S > s.K ? s.S : s.K;
+  const int T = pred_threads(need, s.NB);
+  const int items = (s.NB + T - 1) / T;
+  const PredLayout lay = pred_layout(s);
+#define OASIS_TP(N)                                                                             \
+  {                                                                                             \
+    topk_plan_kernel<N><<<s.units(), T, lay.bytes(), st>>>(                                     \
+        scores, topk_ids, step, clock, slot_of_block, block_of_slot, last_used, fetch_block,    \
+        fetch_slot, evict_block, n_fetch, n_evict, s.NB, s.S, s.K, s.cap, capw, s.sink,         \
+        s.local, di.err, lay);                                                                  \
+    return cudaGetLastError();                                                                  \
+  }
+  OASIS_ITEMS_SWITCH(items, OASIS_TP);
 #undef OASIS_TP
-  return cudaErrorInvalidValue;
 }
 
 }  // namespace oasis
