@@ -21,8 +21,13 @@
 // barrier.  The contraction index is permuted so that thread (g, t) of a warp
 // loads 16 contiguous bytes of block g: dims 16p+4t..16p+4t+3 serve k-steps
 // 2p and 2p+1 (A uses the same permutation, so the dot products are unchanged).
-// Each warp handles tiles of 8 consecutive blocks; the grid is sized to one
-// wave of resident CTAs.
+// Balance: the tiles of 8 consecutive blocks of all (request, KV head) units
+// form one list of T tiles; CTA c (one per SM) takes the contiguous range
+// [c*Rt, (c+1)*Rt) and its warps take every 8th tile of it, so every SM
+// streams the same number of bytes whatever NB and the unit count, and one
+// CTA per SM leaves room for the attention kernel's CTA beside it.  A range
+// meets at most kMaxUnits units (Rt is capped so); their query fragments are
+// staged in shared memory once per CTA.
 #include "common.cuh"
 #include "launch.h"
 
@@ -31,6 +36,8 @@ namespace oasis {
 constexpr int kScoreThreads = 256;
 constexpr int kScoreWarps = kScoreThreads / 32;
 constexpr int kScoreStages = 3;  // tiles of 8 blocks in flight per warp (4 KiB each)
+constexpr int kMaxUnits = 2;     // units whose queries one CTA stages
+constexpr int kMinTilesPerCta = 16;
 
 // 16-byte asynchronous global->shared copy (bypasses L1) and its group fences.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -105,33 +112,34 @@ __device__ __forceinline__ void score_tile(const float4 (&v)[8], const float4* s
 template <int MT>
 __global__ void __launch_bounds__(kScoreThreads) score_kernel(
     const uint16_t* __restrict__ q_draft, const float* __restrict__ summ,
-    float* __restrict__ scores, int L, int Hq, int Hkv, int G, int NB, int tpw) {
-  // shared memory: A fragments [mt][p][half][lane], then one ring per warp of
-  // kScoreStages tiles, each [p][lane] float4 (a lane reads back what it copied)
+    float* __restrict__ scores, int L, int Hq, int Hkv, int G, int NB, int T, int Rt) {
+  // shared memory: A fragments [unit][mt][p][half][lane] for the units of the
+  // range, then one ring per warp of kScoreStages tiles, each [p][lane] float4
+  // (a lane reads back what it copied)
   extern __shared__ float4 smem4[];
   float4* sQ = smem4;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
-  float4* ring = smem4 + MT * 8 * 2 * 32 + warp * kScoreStages * 8 * 32;
+  float4* ring = smem4 + kMaxUnits * MT * 8 * 2 * 32 + warp * kScoreStages * 8 * 32;
   const uint32_t ring_s = smem_u32(ring);
-  const int u = blockIdx.y;
-  const int b = u / Hkv, h = u - b * Hkv;
   const int M = L * G;
-
   const int ntiles = (NB + 7) >> 3;
-  const int tile_base = blockIdx.x * kScoreWarps * tpw + warp;
-  const float* base = summ + static_cast<int64_t>(u) * NB * kHeadDim;
-  const int64_t out_off = static_cast<int64_t>(u) * NB;
-  float* out = scores + out_off;
+  const int t_lo = blockIdx.x * Rt;
+  const int t_hi = t_lo + Rt < T ? t_lo + Rt : T;
+  const int ua = t_lo / ntiles, ub = (t_hi - 1) / ntiles;  // ub - ua < kMaxUnits
+  // this warp's tiles: t_lo + warp + kScoreWarps * i
+  const int tpw = t_hi - t_lo > warp ? (t_hi - t_lo - warp + kScoreWarps - 1) / kScoreWarps : 0;
 
   // copies tile i of this warp into stage i % kScoreStages (one commit group per call)
   auto issue = [&](int i) {
-    const int tile = tile_base + kScoreWarps * i;
-    if (i < tpw && tile < ntiles) {
-      const int blk = tile * 8 + g;
+    if (i < tpw) {
+      const int tile = t_lo + warp + kScoreWarps * i;
+      const int u = tile / ntiles;
+      const int blk = (tile - u * ntiles) * 8 + g;
       const int st = i % kScoreStages;
       if (blk < NB) {
-        const float4* src = reinterpret_cast<const float4*>(base + static_cast<int64_t>(blk) * kHeadDim) + t;
+        const float4* src = reinterpret_cast<const float4*>(
+                                summ + (static_cast<int64_t>(u) * NB + blk) * kHeadDim) + t;
 #pragma unroll
         for (int p = 0; p < 8; ++p)
           cp_async16(ring_s + static_cast<uint32_t>(((st * 8 + p) * 32 + lane) * 16), src + 4 * p);
@@ -145,10 +153,13 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(
 #pragma unroll
   for (int i = 0; i < kScoreStages - 1; ++i) issue(i);
 
-  for (int idx = tid; idx < MT * 8 * 2 * 32; idx += kScoreThreads) {
-    const int ln = idx & 31, half = (idx >> 5) & 1, p = (idx >> 6) & 7, mt = idx >> 9;
+  const int per_unit = MT * 8 * 2 * 32;
+  for (int idx = tid; idx < (ub - ua + 1) * per_unit; idx += kScoreThreads) {
+    const int us = idx / per_unit, r = idx - us * per_unit;
+    const int ln = r & 31, half = (r >> 5) & 1, p = (r >> 6) & 7, mt = r >> 9;
     const int row = 16 * mt + (ln >> 2) + 8 * half;
     const int col = 16 * p + 4 * (ln & 3);
+    const int u = ua + us, b = u / Hkv, h = u - b * Hkv;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (row < M) {
       const int l = row / G, gq = row - l * G;
@@ -163,38 +174,43 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(
 
 #pragma unroll 1
   for (int i = 0; i < tpw; ++i) {
-    const int tile = tile_base + kScoreWarps * i;
-    if (tile >= ntiles) break;
+    const int tile = t_lo + warp + kScoreWarps * i;
+    const int u = tile / ntiles;
     issue(i + kScoreStages - 1);
     cp_async_wait<kScoreStages - 1>();  // tile i has landed (this lane's copies)
     const int st = i % kScoreStages;
     float4 v[8];
 #pragma unroll
     for (int p = 0; p < 8; ++p) v[p] = ring[(st * 8 + p) * 32 + lane];
-    score_tile<MT>(v, sQ, lane, g, t, M, tile * 8, NB, out_off, out);
+    const int64_t out_off = static_cast<int64_t>(u) * NB;
+    score_tile<MT>(v, sQ + (u - ua) * per_unit, lane, g, t, M, (tile - u * ntiles) * 8, NB,
+                   out_off, scores + out_off);
   }
   cp_async_wait<0>();
 }
 
 static size_t score_smem_bytes(int mt) {
-  return sizeof(float4) * (static_cast<size_t>(mt) * 8 * 2 * 32 + kScoreWarps * kScoreStages * 8 * 32);
+  return sizeof(float4) * (static_cast<size_t>(kMaxUnits) * mt * 8 * 2 * 32 +
+                           kScoreWarps * kScoreStages * 8 * 32);
 }
 
 template <int MT>
 static cudaError_t launch_mt(const Shape& s, const uint16_t* q_draft, const float* summ,
                              float* scores, cudaStream_t st, const DeviceInfo& di) {
-  // one wave: as many CTAs per (request, KV head) as the resident CTA slots allow
+  // one CTA per SM over equal contiguous tile ranges, each range meeting at
+  // most kMaxUnits units
   const int ntiles = (s.NB + 7) / 8;
-  const int per_sm = di.score_ctas_per_sm > 0 ? di.score_ctas_per_sm : 2;
-  const int64_t slots = static_cast<int64_t>(di.sm_count > 0 ? di.sm_count : 148) * per_sm;
-  int cpu = static_cast<int>(slots / s.units());
-  if (cpu < 1) cpu = 1;
-  int tpw = (ntiles + kScoreWarps * cpu - 1) / (kScoreWarps * cpu);
-  if (tpw < 1) tpw = 1;
-  const int ctas_per_unit = (ntiles + kScoreWarps * tpw - 1) / (kScoreWarps * tpw);
-  dim3 grid(ctas_per_unit, s.units());
-  score_kernel<MT><<<grid, kScoreThreads, score_smem_bytes(MT), st>>>(q_draft, summ, scores, s.L, s.Hq, s.Hkv,
-                                                      s.G, s.NB, tpw);
+  const int64_t T = static_cast<int64_t>(s.units()) * ntiles;
+  int64_t C = di.sm_count > 0 ? di.sm_count : 148;
+  const int64_t cap = (T + kMinTilesPerCta - 1) / kMinTilesPerCta;
+  if (C > cap) C = cap;
+  if (C < 1) C = 1;
+  int64_t Rt = (T + C - 1) / C;
+  const int64_t rmax = static_cast<int64_t>(kMaxUnits - 1) * ntiles + 1;
+  if (Rt > rmax) Rt = rmax;
+  const int64_t grid = (T + Rt - 1) / Rt;
+  score_kernel<MT><<<static_cast<unsigned>(grid), kScoreThreads, score_smem_bytes(MT), st>>>(
+      q_draft, summ, scores, s.L, s.Hq, s.Hkv, s.G, s.NB, static_cast<int>(T), static_cast<int>(Rt));
   return cudaGetLastError();
 }
 

@@ -266,6 +266,17 @@ def test_attention_shapes_masks_and_empty_slots():
     _attn_case(small_wl(num_q_heads=6, num_kv_heads=2), seed=7, scale=0.5)                       # G = 3
 
 
+def test_attention_units_inside_one_warp_and_long_units():
+    # many short units: several lie wholly inside one warp's slot range and are
+    # finished from registers, others straddle two warps and are merged
+    _attn_case(small_wl(batch=40, num_q_heads=32, num_kv_heads=8, kv_budget_tokens=16 * 3, top_k=3),
+               seed=10, empty_frac=0.2)
+    _attn_case(small_wl(batch=64, num_q_heads=16, num_kv_heads=8, kv_budget_tokens=16 * 2, top_k=2), seed=11)
+    # one unit spread over hundreds of warps (G = 8): merged in several rounds
+    _attn_case(small_wl(batch=1, num_q_heads=16, num_kv_heads=2, ctx_tokens=16 * 2048,
+                        kv_budget_tokens=16 * 1024, top_k=64), seed=12, empty_frac=0.1)
+
+
 def test_attention_empty_and_fully_masked_give_zeros():
     wl = small_wl()
     out, ref = _attn_case(wl, seed=8, empty_frac=1.0)

@@ -12,7 +12,6 @@ inputs, and checks each output against the ordinary call with its own
 workspace, within the attention tolerance the other GPU tests use.  It must
 pass both on its own in a fresh process and after every other test.
 """
-import ctypes as C
 import math
 
 import numpy as np
@@ -71,14 +70,14 @@ def test_no_alloc_attention_matches_workspace_call_twice(wl):
     assert ob.oasis_device_errors() == 0
 
 
-def test_no_alloc_attention_rejects_configs_beyond_its_scratch():
-    """A shape whose scratch exceeds the fixed 8 MiB is refused before any launch."""
-    big = W.Workload(name="too-big", batch=64, num_q_heads=64, num_kv_heads=8, ctx_tokens=16 * 4096,
-                     kv_budget_tokens=16 * 1024, lookahead=1, top_k=64, fetch_ratio=0.05, seed=1)
+def test_no_alloc_scratch_covers_the_largest_valid_shape():
+    """The scratch holds two partials per warp of one CTA per SM plus one
+    counter per unit, so the largest shape the library accepts fits in the
+    fixed 8 MiB; the call's size guard (OASIS_ERR_UNSUPPORTED) never fires
+    for a valid configuration on this part."""
+    big = W.Workload(name="largest", batch=8191, num_q_heads=64, num_kv_heads=8,
+                     ctx_tokens=16 * 32768, kv_budget_tokens=16 * 1024, lookahead=1, top_k=1024,
+                     fetch_ratio=0.05, seed=1)
     assert ob.oasis_validate_config(big) == ob.OASIS_OK
-    assert ob.oasis_attn_workspace_bytes(big) > 8 << 20
-    buf = torch.zeros((64, 64, 128), dtype=torch.bfloat16, device="cuda")  # never read
-    p = C.c_void_p(buf.data_ptr())
-    st = ob.lib().oasis_sparse_decode_attn_static(C.byref(ob.OasisConfig.make(big)), p, p, p, p,
-                                                  None, 0.1, p, None)
-    assert st == ob.OASIS_ERR_UNSUPPORTED
+    assert big.batch * big.num_kv_heads <= 65535
+    assert ob.oasis_attn_workspace_bytes(big) <= 8 << 20
