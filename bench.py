@@ -329,6 +329,20 @@ def gpu_arm(args):
         fork.record(compute)
         joins = []
 
+        # the attention (the longest branch) is enqueued first
+        if "attn" in active:
+            i, qi = qset(s)
+            L = layers[i]
+            if host_io:
+                q_in[i].copy_(q_host[i][qi], non_blocking=True)
+                qd_in[i].copy_(qd_host[i][qi], non_blocking=True)
+                q = q_in[i]
+            else:
+                q = q_dev[i][qi]
+            L.attention(q, compute)
+            if host_io:
+                out_host[i].copy_(L.out, non_blocking=True)
+
         def branch(stream, fn):
             stream.wait_event(fork)
             fn(stream)
@@ -350,18 +364,6 @@ def gpu_arm(args):
         if "fetch" in active:
             L3 = layers[(s - 3) % n_inst]
             branch(copy, lambda st: L3.fetch(st))
-        if "attn" in active:
-            i, qi = qset(s)
-            L = layers[i]
-            if host_io:
-                q_in[i].copy_(q_host[i][qi], non_blocking=True)
-                qd_in[i].copy_(qd_host[i][qi], non_blocking=True)
-                q = q_in[i]
-            else:
-                q = q_dev[i][qi]
-            L.attention(q, compute)
-            if host_io:
-                out_host[i].copy_(L.out, non_blocking=True)
         for e in joins:
             compute.wait_event(e)
 

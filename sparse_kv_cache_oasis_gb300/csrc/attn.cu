@@ -21,16 +21,18 @@
 //     fragments come from the swizzled tiles with ldmatrix / ldmatrix.trans;
 //     P^T is the S^T accumulator rounded to bf16 and transposed in registers
 //     with movmatrix.  Online softmax in base 2, fp32 state (max m, sum l).
-//   - A unit whose slots all lie in one warp's range is finished by that warp
-//     straight from its registers.  A unit shared by several warps (at most
-//     the first and the last unit of a warp's range) gets one fp32 partial
-//     (m, l, O) per warp; each warp then adds the number of the unit's slots it
-//     covered to the unit's counter, and the warp that brings it to S merges
-//     the unit: bulk copies of the partials into its own (now idle) ring, then
-//     per head a warp-wide max, one weight per partial and a weighted sum of
-//     the O columns in shared memory, bf16 out, and the counter back to zero
-//     for the next call.  The workspace is therefore two partials
-//     per warp plus one counter per unit, whatever the shape.
+//   - Merging (split slot ranges, online-softmax partials (m, l, O) in fp32):
+//     a unit whose slots all lie in one warp's range is finished by that warp
+//     from its registers.  Otherwise each warp parks its partial for the unit
+//     in its own ring (idle once its copies have landed); after one CTA
+//     barrier the warps fold the parked partials, one (unit, head) pair per
+//     warp at a time: a unit inside the CTA's range is finished there, a unit
+//     crossing the range's edge (at most the first and the last) leaves one
+//     CTA partial in the workspace.  Each CTA then adds the number of such a
+//     unit's slots it covered to the unit's counter; the CTA that brings it to
+//     S folds the unit's CTA partials from L2, writes bf16 out and puts the
+//     counter back to zero for the next call.  The workspace is two partials
+//     per CTA plus one counter per unit, whatever the shape.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -49,7 +51,7 @@ constexpr int kMaxGroup = kMaxAttnGroup;
 constexpr int kPartFloats = kMaxGroup * kPartStride;  // one partial (all heads)
 constexpr int kMinSlotsPerCta = 16;
 constexpr size_t kAttnSmem = 1024 + static_cast<size_t>(kAttnWarps) * kRingBytes +
-                             static_cast<size_t>(kAttnWarps) * (kStages + 1) * 8;
+                             static_cast<size_t>(kAttnWarps) * kStages * 8;
 
 // ------------------------------------------------------------ static partition
 struct Part {
@@ -88,9 +90,9 @@ static int current_sm_count() {
   return n;
 }
 
-// two partials (first and last unit of the range) per warp
+// two partials (the units crossing the range's left and right edges) per CTA
 static size_t partial_bytes(const Part& pt) {
-  return static_cast<size_t>(part_ctas(pt)) * kAttnWarps * 2 * kPartFloats * sizeof(float);
+  return static_cast<size_t>(part_ctas(pt)) * 2 * kPartFloats * sizeof(float);
 }
 static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -131,19 +133,17 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(
   const int c = blockIdx.x;
   int wa, wb;
   pt.warp_range(c, warp, &wa, &wb);
-  if (wa >= wb) return;  // an empty quarter (tiny ranges only): nothing to stream or count
+  const bool has_work = wa < wb;  // a quarter can be empty for tiny ranges
 
   uint8_t* ring = smem + static_cast<size_t>(warp) * kRingBytes;
   const uint32_t ring_s = smem_u32(ring);
   const uint32_t bars = smem_u32(smem + static_cast<size_t>(kAttnWarps) * kRingBytes);
   const uint32_t bar0 = bars + 8 * kStages * warp;
-  const uint32_t mbar = bars + 8 * kStages * kAttnWarps + 8 * warp;  // merge copies
 
   if (lane == 0) {
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
     for (int st = 0; st < kStages; ++st) mbar_init(bar0 + 8 * st, 1);
-    mbar_init(mbar, 1);
     fence_mbar_init();
     fence_proxy_async_smem();
   }
@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(
   // ---- issue cursor over the valid slots of [wa, wb), 32 slots at a time
   int cur_base = wa - 32, cur_blk = -1;
   unsigned cur_mask = 0u;
-  bool exhausted = false;
+  bool exhausted = !has_work;
   int issued = 0, rj = -1, rb = -1;  // lane k keeps (slot, block) of the entries k mod kStages
   auto try_issue = [&]() {
     while (cur_mask == 0u) {
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(
   while (issued < kStages && !exhausted) try_issue();
 
   // ---- per-unit online-softmax state
-  const int uf = wa / S, ul = (wb - 1) / S;  // first and last unit of the range
+  const int uf = wa / S, ul = has_work ? (wb - 1) / S : uf - 1;  // first and last unit of the range
   auto owned = [&](int u) { return u * S >= wa && u * S + S <= wb; };
   const int k_row = (lane & 7) + 8 * ((lane >> 3) & 1);
   const int k_hi = lane >> 4;
@@ -224,11 +224,35 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(
     m_e = m_o = -INFINITY;
     l_e = l_o = 0.f;
   };
+  // A shared first unit is finished mid-stream, while copies are still landing
+  // in the ring: its partial is held in registers until the stream is done.
+  float ho_[8][4];
+  float hm_e = -INFINITY, hm_o = -INFINITY, hl_e = 0.f, hl_o = 0.f;
+  bool held = false;
+  // parks a partial in slot `side` of this warp's ring (free once the stream is done)
+  auto park = [&](int side, const float (&ov)[8][4], float me, float mo, float le, float lo) {
+    float* pe = reinterpret_cast<float*>(ring) + side * kPartFloats + (2 * t) * kPartStride;
+    float* po = pe + kPartStride;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      pe[4 + 16 * mt + g] = ov[mt][0];
+      po[4 + 16 * mt + g] = ov[mt][1];
+      pe[4 + 16 * mt + g + 8] = ov[mt][2];
+      po[4 + 16 * mt + g + 8] = ov[mt][3];
+    }
+    if (g == 0) {
+      pe[0] = me;
+      pe[1] = le;
+      po[0] = mo;
+      po[1] = lo;
+    }
+  };
   // Hands on the state of cur_u: the output itself when this warp owns the
-  // whole unit, else the warp's partial for it.
+  // whole unit, else the warp's partial for it (held, or parked when it is
+  // the last unit, which is only finished after the stream).
   auto flush = [&]() {
     const float le = warp_sum_xor_g(l_e), lo_ = warp_sum_xor_g(l_o);
-    const int he = 2 * t, ho = 2 * t + 1;  // the two heads of this lane's columns
+    const int he = 2 * t, hoo = 2 * t + 1;  // the two heads of this lane's columns
     if (owned(cur_u)) {
       const int b = cur_u / Hkv, h = cur_u - b * Hkv;
       const float ie = le > 0.f ? 1.f / le : 0.f, io = lo_ > 0.f ? 1.f / lo_ : 0.f;
@@ -240,35 +264,32 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(
           oe[16 * mt + g] = bf16_bits(o[mt][0] * ie);
           oe[16 * mt + g + 8] = bf16_bits(o[mt][2] * ie);
         }
-        if (ho < G) {
+        if (hoo < G) {
           oo[16 * mt + g] = bf16_bits(o[mt][1] * io);
           oo[16 * mt + g + 8] = bf16_bits(o[mt][3] * io);
         }
       }
-      return;
-    }
-    const int side = cur_u == uf ? 0 : 1;
-    float* pe = ws_part + ((static_cast<int64_t>(c) * kAttnWarps + warp) * 2 + side) * kPartFloats +
-                he * kPartStride;
-    float* po = pe + kPartStride;
+    } else if (cur_u == uf) {
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      pe[4 + 16 * mt + g] = o[mt][0];
-      po[4 + 16 * mt + g] = o[mt][1];
-      pe[4 + 16 * mt + g + 8] = o[mt][2];
-      po[4 + 16 * mt + g + 8] = o[mt][3];
-    }
-    if (g == 0) {
-      pe[0] = m_e;
-      pe[1] = le;
-      po[0] = m_o;
-      po[1] = lo_;
+      for (int mt = 0; mt < 8; ++mt) {
+        ho_[mt][0] = o[mt][0];
+        ho_[mt][1] = o[mt][1];
+        ho_[mt][2] = o[mt][2];
+        ho_[mt][3] = o[mt][3];
+      }
+      hm_e = m_e;
+      hm_o = m_o;
+      hl_e = le;
+      hl_o = lo_;
+      held = true;
+    } else {
+      park(1, o, m_e, m_o, le, lo_);
     }
   };
 
   bool ok = true;
   int consumed = 0;
-  begin_unit(uf);
+  if (has_work) begin_unit(uf);
 #pragma unroll 1
   while (consumed < issued) {
     const int st = consumed % kStages;
@@ -335,129 +356,177 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(
     // let the copies still in flight land before the ring is reused or released
     for (int i = consumed; i < issued; ++i)
       (void)mbar_wait_bounded(bar0 + 8 * (i % kStages), (i / kStages) & 1);
-  } else {
-    while (true) {  // the last unit, and any trailing units without a valid slot
+  } else if (has_work) {
+    // the last unit, and any trailing units without a valid slot (all
+    // streaming copies have landed, so the ring is free for the partials)
+    while (true) {
       flush();
       if (cur_u >= ul) break;
       begin_unit(cur_u + 1);
     }
+    if (held) park(0, ho_, hm_e, hm_o, hl_e, hl_o);
   }
 
-  // ---- count in for the shared first and last units (lanes 0 and 1).  A warp
-  //      counts in even after a timed-out wait (the error word is set) so that
-  //      the counters return to zero.
-  __threadfence();  // the partials above, before the count
-  __syncwarp();
-  int mine = -1;
-  bool last = false;
-  if ((lane == 0 && !owned(uf)) || (lane == 1 && ul != uf && !owned(ul))) {
-    mine = lane == 0 ? uf : ul;
-    const int lo = wa > mine * S ? wa : mine * S;
-    const int hi = wb < mine * S + S ? wb : mine * S + S;
-    last = atomicAdd(ws_cnt + mine, hi - lo) + (hi - lo) == S;
-  }
-  unsigned lm = __ballot_sync(0xffffffffu, last);
-  int phase = 0;
+  // ---- CTA level: fold the warps' parked partials unit by unit.  A unit that
+  //      lies inside the CTA's range is finished here; one that crosses its
+  //      edge (at most the first and the last) leaves one CTA partial in the
+  //      workspace.  Tasks are (unit, head) pairs, spread over the warps.
+  __syncthreads();
+  const int ca = pt.start(c), cb = pt.start(c + 1);
+  const int ua = ca / S, ub = (cb - 1) / S;
+  const float* rings = reinterpret_cast<const float*>(smem);
+  constexpr int kRingFloats = kRingBytes / static_cast<int>(sizeof(float));
+  const int nu = ub - ua + 1;
 #pragma unroll 1
-  while (lm) {
-    const int u = __shfl_sync(0xffffffffu, mine, __ffs(lm) - 1);
-    lm &= lm - 1;
-    __threadfence();          // the other warps' partials, after their counts
-    fence_proxy_async_all();  // ... and before the bulk copies read them
-    const int b = u / Hkv, h = u - b * Hkv;
-    const int ua = u * S, ub = ua + S;
-    const int c_lo = ua / R, c_hi = (ub - 1) / R;
-    const int ncand = (c_hi - c_lo + 1) * kAttnWarps;
-    // Rounds of bulk copies into this warp's ring: slot 0 keeps the merge of
-    // the rounds before (in the partial's own format), the other slots take
-    // new partials.  Each round folds all its slots at once: a warp-wide max
-    // and weight per partial, then a weighted sum of the O columns.
-    const int row_floats = G * kPartStride;
-    const uint32_t row_bytes = static_cast<uint32_t>(row_floats) * sizeof(float);
-    const int cap = kRingBytes / static_cast<int>(row_bytes);  // partials the ring holds (>= 5)
-    float* ring_f = reinterpret_cast<float*>(ring);
-    int held = 0;
-    bool merge_ok = true;
-#pragma unroll 1
-    for (int base = 0; base < ncand && merge_ok; base += 32) {
-      // lane i looks at candidate warp base+i of the CTAs meeting the unit
-      const int i = base + lane;
-      int off = -1;
-      if (i < ncand) {
-        const int cc = c_lo + i / kAttnWarps, ww = i % kAttnWarps;
-        int lo, hi;
-        pt.warp_range(cc, ww, &lo, &hi);
-        if (lo < hi && lo < ub && hi > ua)
-          off = ((cc * kAttnWarps + ww) * 2 + (lo / S == u ? 0 : 1)) * kPartFloats;
-      }
-      unsigned cm = __ballot_sync(0xffffffffu, off >= 0);
-#pragma unroll 1
-      while (cm) {
-        unsigned take = 0u;
-        int n = 0;
-        for (unsigned rest = cm; rest && n < cap - held; rest &= rest - 1, ++n)
-          take |= rest & (~rest + 1u);
-        cm &= ~take;
-        __syncwarp();
-        if (lane == 0) {
-          fence_proxy_async_smem();  // earlier reads of the ring, before the copies
-          mbar_arrive_expect_tx(mbar, n * row_bytes);
-        }
-        __syncwarp();
-        if (take & (1u << lane)) {
-          const int rank = __popc(take & ((1u << lane) - 1u));
-          bulk_load(ring_s + (held + rank) * row_bytes, ws_part + off, row_bytes, mbar);
-        }
-        const bool landed = mbar_wait_bounded(mbar, phase & 1);
-        ++phase;
-        if (!__all_sync(0xffffffffu, landed)) {
-          if (lane == 0) set_error(err, OASIS_DEVERR_WAIT_TIMEOUT);
-          (void)mbar_wait_bounded(mbar, (phase - 1) & 1);
-          merge_ok = false;
-          break;
-        }
-        const int nn = held + n;
-        const bool final_round = cm == 0u && base + 32 >= ncand;
-#pragma unroll 1
-        for (int hd = 0; hd < G; ++hd) {
-          float* ph = ring_f + hd * kPartStride;  // row hd of slot 0; slot k is k * row_floats on
-          const float mk = lane < nn ? ph[lane * row_floats] : -INFINITY;
-          const float lk = lane < nn ? ph[lane * row_floats + 1] : 0.f;
-          float mx = mk;
+  for (int task = warp; task < nu * G; task += kAttnWarps) {
+    const int u = ua + task / G, hd = task - (task / G) * G;
+    const int us = u * S, ue = us + S;
+    unsigned wm = 0u;
+    bool warp_done = false;
 #pragma unroll
-          for (int d = 16; d > 0; d >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
-          const float wk = mk == -INFINITY ? 0.f : exp2f(mk - mx);
-          float ls = wk * lk;
-#pragma unroll
-          for (int d = 16; d > 0; d >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, d);
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int k = 0; k < nn; ++k) {
-            const float w = __shfl_sync(0xffffffffu, wk, k);
-            const float4 v = *reinterpret_cast<const float4*>(ph + k * row_floats + 4 + 4 * lane);
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
-          }
-          if (final_round) {
-            const float inv = ls > 0.f ? 1.f / ls : 0.f;
-            uint2 pk;
-            pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-            pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-            *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(b) * Hq + h * G + hd) * kHeadDim +
-                                      4 * lane) = pk;
-          } else {  // each lane rewrites only what it alone read: its column and, lane 0, m and l
-            *reinterpret_cast<float4*>(ph + 4 + 4 * lane) = acc;
-            if (lane == 0) {
-              ph[0] = mx;
-              ph[1] = ls;
-            }
-          }
-        }
-        held = 1;
+    for (int w = 0; w < kAttnWarps; ++w) {
+      int lo, hi;
+      pt.warp_range(c, w, &lo, &hi);
+      if (lo < hi && lo < ue && hi > us) {
+        wm |= 1u << w;
+        warp_done = lo <= us && ue <= hi;  // that warp owned the unit and wrote it out
       }
     }
-    if (lane == 0) ws_cnt[u] = 0;
+    if (warp_done) continue;
+    // two-pass fold over at most kAttnWarps partials: max, weights, sums
+    float mw[kAttnWarps], lw[kAttnWarps];
+    float4 ow[kAttnWarps];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) {
+      mw[w] = -INFINITY;
+      lw[w] = 0.f;
+      ow[w] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (wm & (1u << w)) {
+        int lo, hi;
+        pt.warp_range(c, w, &lo, &hi);
+        const float* p = rings + w * kRingFloats + (lo / S == u ? 0 : kPartFloats) + hd * kPartStride;
+        mw[w] = p[0];
+        lw[w] = p[1];
+        ow[w] = *reinterpret_cast<const float4*>(p + 4 + 4 * lane);
+        mx = fmaxf(mx, mw[w]);
+      }
+    }
+    float ls = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) {
+      const float wt = mw[w] == -INFINITY ? 0.f : exp2f(mw[w] - mx);
+      ls += wt * lw[w];
+      acc.x += wt * ow[w].x;
+      acc.y += wt * ow[w].y;
+      acc.z += wt * ow[w].z;
+      acc.w += wt * ow[w].w;
+    }
+    if (us >= ca && ue <= cb) {  // inside the CTA's range: final
+      const int b = u / Hkv, h = u - b * Hkv;
+      const float inv = ls > 0.f ? 1.f / ls : 0.f;
+      uint2 pk;
+      pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+      pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(b) * Hq + h * G + hd) * kHeadDim +
+                                4 * lane) = pk;
+    } else {
+      float* q_ = ws_part + (static_cast<int64_t>(c) * 2 + (u == ua ? 0 : 1)) * kPartFloats +
+                  hd * kPartStride;
+      *reinterpret_cast<float4*>(q_ + 4 + 4 * lane) = acc;
+      if (lane == 0) {
+        q_[0] = mx;
+        q_[1] = ls;
+      }
+    }
+  }
+
+  // ---- count in for the edge units (lanes 0 and 1 of warp 0): each CTA adds
+  //      the number of the unit's slots it covered; the CTA that brings the
+  //      count to S merges the unit and puts the counter back to zero.  A CTA
+  //      counts in even after a timed-out wait (the error word is set) so that
+  //      the counters return to zero.
+  __shared__ int sMerge[2];
+  __threadfence();  // this CTA's partials, before its count
+  __syncthreads();
+  if (warp == 0) {
+    int u = -1;
+    if (lane == 0 && ua * S < ca) u = ua;
+    if (lane == 1 && (ub + 1) * S > cb && (ub != ua || ua * S >= ca)) u = ub;
+    bool last = false;
+    if (u >= 0) {
+      const int lo = ca > u * S ? ca : u * S;
+      const int hi = cb < u * S + S ? cb : u * S + S;
+      last = atomicAdd(ws_cnt + u, hi - lo) + (hi - lo) == S;
+    }
+    if (lane < 2) sMerge[lane] = last ? u : -1;
+  }
+  __syncthreads();
+  const int m0 = sMerge[0], m1 = sMerge[1];
+  if (m0 < 0 && m1 < 0) return;
+  __threadfence();  // the other CTAs' partials, after their counts
+  const int nm = (m0 >= 0) + (m1 >= 0);
+#pragma unroll 1
+  for (int task = warp; task < nm * G; task += kAttnWarps) {
+    const int u = (task / G == 0 && m0 >= 0) ? m0 : m1;
+    const int hd = task - (task / G) * G;
+    const int b = u / Hkv, h = u - b * Hkv;
+    const int c_lo = (u * S) / R, c_hi = (u * S + S - 1) / R;
+    float M = -INFINITY, L = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int kBatch = 8;
+#pragma unroll 1
+    for (int c0 = c_lo; c0 <= c_hi; c0 += kBatch) {
+      float mv[kBatch], lv[kBatch];
+      float4 ov[kBatch];
+      float bm = M;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        mv[k] = -INFINITY;
+        lv[k] = 0.f;
+        ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int cc = c0 + k;
+        if (cc <= c_hi) {
+          const float* p = ws_part +
+                           (static_cast<int64_t>(cc) * 2 + (pt.start(cc) / S == u ? 0 : 1)) * kPartFloats +
+                           hd * kPartStride;
+          mv[k] = __ldcg(p);
+          lv[k] = __ldcg(p + 1);
+          ov[k] = __ldcg(reinterpret_cast<const float4*>(p + 4 + 4 * lane));
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) bm = fmaxf(bm, mv[k]);
+      if (bm != -INFINITY) {
+        const float r = exp2f(M - bm);  // 0 while M is -inf
+        L *= r;
+        O.x *= r;
+        O.y *= r;
+        O.z *= r;
+        O.w *= r;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          const float wt = mv[k] == -INFINITY ? 0.f : exp2f(mv[k] - bm);
+          L += wt * lv[k];
+          O.x += wt * ov[k].x;
+          O.y += wt * ov[k].y;
+          O.z += wt * ov[k].z;
+          O.w += wt * ov[k].w;
+        }
+        M = bm;
+      }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    uint2 pk;
+    pk.x = pack_bf16x2(O.x * inv, O.y * inv);
+    pk.y = pack_bf16x2(O.z * inv, O.w * inv);
+    *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(b) * Hq + h * G + hd) * kHeadDim +
+                              4 * lane) = pk;
+  }
+  if (threadIdx.x == 0) {
+    if (m0 >= 0) ws_cnt[m0] = 0;
+    if (m1 >= 0) ws_cnt[m1] = 0;
   }
 }
 

@@ -9,9 +9,11 @@
 // workloads' shapes), which is at or above the fp32 CUDA-core rate at full
 // HBM bandwidth, so it runs on the tensor cores:
 //   - A = queries: bf16 values are exact in tf32;
-//   - B = summaries: fp32 split as hi = tf32(x), lo = tf32(x - hi) (x - hi is
-//     exact), two MMA passes; the product error is ~2^-22 relative, far
-//     below the fp32 result rounding that ranking depends on;
+//   - B = summaries: fp32 split as hi = x with its 13 low mantissa bits
+//     cleared (exactly a tf32 value) and lo = x - hi (exact in fp32; the
+//     tensor core reads it as tf32, dropping at most 2^-11 of it), two MMA
+//     passes; the product error is ~2^-21 relative, far below the fp32 result
+//     rounding that ranking depends on;
 //   - mma.sync m16n8k8 tf32 with fp32 accumulation, one 16-row tile per 16
 //     query rows.
 // Memory path: summaries are streamed once with 16-byte cp.async copies into
@@ -51,22 +53,28 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
+constexpr uint32_t kTf32Mask = 0xFFFFE000u;  // sign, exponent, 10 mantissa bits
+
 // Scores of 8 blocks (one tile) from their summaries in v; writes them out.
 template <int MT>
 __device__ __forceinline__ void score_tile(const float4 (&v)[8], const float4* sQ, int lane, int g,
                                            int t, int M, int n0, int NB, int64_t out_off,
                                            float* out) {
-  float acc[MT][4];
+  // four independent accumulator chains (hi/lo x even/odd k-step) keep the
+  // MMA dependency chains short; they are summed at the end
+  float acc[MT][4], acc1[MT][4], acc2[MT][4], acc3[MT][4];
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[mt][r] = acc1[mt][r] = acc2[mt][r] = acc3[mt][r] = 0.f;
 #pragma unroll
   for (int p = 0; p < 8; ++p) {
-    const uint32_t hx = to_tf32(v[p].x), hy = to_tf32(v[p].y);
-    const uint32_t hz = to_tf32(v[p].z), hw = to_tf32(v[p].w);
-    const uint32_t lx = to_tf32(v[p].x - __uint_as_float(hx));
-    const uint32_t ly = to_tf32(v[p].y - __uint_as_float(hy));
-    const uint32_t lz = to_tf32(v[p].z - __uint_as_float(hz));
-    const uint32_t lw = to_tf32(v[p].w - __uint_as_float(hw));
+    const uint32_t hx = __float_as_uint(v[p].x) & kTf32Mask, hy = __float_as_uint(v[p].y) & kTf32Mask;
+    const uint32_t hz = __float_as_uint(v[p].z) & kTf32Mask, hw = __float_as_uint(v[p].w) & kTf32Mask;
+    const uint32_t lx = __float_as_uint(v[p].x - __uint_as_float(hx));
+    const uint32_t ly = __float_as_uint(v[p].y - __uint_as_float(hy));
+    const uint32_t lz = __float_as_uint(v[p].z - __uint_as_float(hz));
+    const uint32_t lw = __float_as_uint(v[p].w - __uint_as_float(hw));
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       const float4 qa = sQ[((mt * 8 + p) * 2 + 0) * 32 + lane];
@@ -75,12 +83,16 @@ __device__ __forceinline__ void score_tile(const float4 (&v)[8], const float4* s
       const uint32_t a2 = __float_as_uint(qa.y), a3 = __float_as_uint(qb.y);
       const uint32_t c0 = __float_as_uint(qa.z), c1 = __float_as_uint(qb.z);
       const uint32_t c2 = __float_as_uint(qa.w), c3 = __float_as_uint(qb.w);
-      mma_tf32_1688(acc[mt], a0, a1, a2, a3, hx, hy);  // k-step 2p, hi
-      mma_tf32_1688(acc[mt], a0, a1, a2, a3, lx, ly);  // k-step 2p, lo
-      mma_tf32_1688(acc[mt], c0, c1, c2, c3, hz, hw);  // k-step 2p+1, hi
-      mma_tf32_1688(acc[mt], c0, c1, c2, c3, lz, lw);  // k-step 2p+1, lo
+      mma_tf32_1688(acc[mt], a0, a1, a2, a3, hx, hy);   // k-step 2p, hi
+      mma_tf32_1688(acc1[mt], a0, a1, a2, a3, lx, ly);  // k-step 2p, lo
+      mma_tf32_1688(acc2[mt], c0, c1, c2, c3, hz, hw);  // k-step 2p+1, hi
+      mma_tf32_1688(acc3[mt], c0, c1, c2, c3, lz, lw);  // k-step 2p+1, lo
     }
   }
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[mt][r] = (acc[mt][r] + acc2[mt][r]) + (acc1[mt][r] + acc3[mt][r]);
   // max over the valid query rows (rows >= L*G are padding)
   float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
