@@ -309,6 +309,8 @@ def gpu_arm(args):
     score_st = torch.cuda.Stream(device=dev)
     select_st = torch.cuda.Stream(device=dev)
     copy = torch.cuda.Stream(device=dev, priority=-1)
+    h2d = torch.cuda.Stream(device=dev)
+    d2h = torch.cuda.Stream(device=dev)
     out_host = [torch.empty_like(L.out, device="cpu").pin_memory() for L in layers]
     q_in = [torch.empty_like(q_dev[i][0]) for i in range(n_inst)]
     qd_in = [torch.empty_like(qd_dev[i][0]) for i in range(n_inst)]
@@ -324,24 +326,13 @@ def gpu_arm(args):
         s-3, each on its own stream.  `active` = which of the four run (the
         first and last graphs of a run fill and drain the pipeline).  The four
         steps use four different layer copies, and each one's inputs were
-        produced by an earlier graph."""
+        produced by an earlier graph.  With host I/O, step s+1's queries are
+        copied in from pinned host memory and step s-1's output is copied out
+        beside step s's kernels (a run's first step copies its own queries in
+        before its attention)."""
         fork = torch.cuda.Event()
         fork.record(compute)
         joins = []
-
-        # the attention (the longest branch) is enqueued first
-        if "attn" in active:
-            i, qi = qset(s)
-            L = layers[i]
-            if host_io:
-                q_in[i].copy_(q_host[i][qi], non_blocking=True)
-                qd_in[i].copy_(qd_host[i][qi], non_blocking=True)
-                q = q_in[i]
-            else:
-                q = q_dev[i][qi]
-            L.attention(q, compute)
-            if host_io:
-                out_host[i].copy_(L.out, non_blocking=True)
 
         def branch(stream, fn):
             stream.wait_event(fork)
@@ -350,6 +341,20 @@ def gpu_arm(args):
             e.record(stream)
             joins.append(e)
 
+        def copy_in(stream, step):
+            i, qi = qset(step)
+            with torch.cuda.stream(stream):
+                q_in[i].copy_(q_host[i][qi], non_blocking=True)
+                qd_in[i].copy_(qd_host[i][qi], non_blocking=True)
+
+        if "h2d_now" in active:
+            branch(h2d, lambda st: copy_in(st, s))
+            compute.wait_event(joins.pop())
+        # the attention (the longest branch) is enqueued first
+        if "attn" in active:
+            i, qi = qset(s)
+            L = layers[i]
+            L.attention(q_in[i] if host_io else q_dev[i][qi], compute)
         if "score" in active:
             i1, qi1 = qset(s - 1)
             qd = qd_in[i1] if host_io else qd_dev[i1][qi1]
@@ -364,14 +369,30 @@ def gpu_arm(args):
         if "fetch" in active:
             L3 = layers[(s - 3) % n_inst]
             branch(copy, lambda st: L3.fetch(st))
+        if "h2d_next" in active:
+            branch(h2d, lambda st: copy_in(st, s + 1))
+        if "d2h_prev" in active:
+            ip = (s - 1) % n_inst
+
+            def copy_out(st):
+                with torch.cuda.stream(st):
+                    out_host[ip].copy_(layers[ip].out, non_blocking=True)
+            branch(d2h, copy_out)
         for e in joins:
             compute.wait_event(e)
 
-    def active_of(s, s0, n):
+    def active_of(s, s0, n, host_io=False):
         parts = []
         for name, lag in (("attn", 0), ("score", 1), ("select", 2), ("fetch", 3)):
             if s0 <= s - lag < s0 + n:
                 parts.append(name)
+        if host_io:
+            if s == s0:
+                parts.append("h2d_now")
+            if s0 <= s + 1 < s0 + n:
+                parts.append("h2d_next")
+            if s0 <= s - 1 < s0 + n:
+                parts.append("d2h_prev")
         return frozenset(parts)
 
     # ---- warm the library (first calls set up per-device state)
@@ -391,20 +412,46 @@ def gpu_arm(args):
             graphs[key] = g
         return graphs[key]
 
+    # Steady-state steps are replayed n_inst at a time (one graph per cycle of
+    # the layer copies) to keep the host's launch cost per step small; the
+    # pipeline's fill and drain use one graph per step.
+    def full_mask(host_io):
+        return frozenset(("attn", "score", "select", "fetch")
+                         + (("h2d_next", "d2h_prev") if host_io else ()))
+
+    def chunk_graph(s, host_io):
+        key = ("chunk", s % period, host_io)
+        if key not in graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=compute):
+                for k in range(n_inst):
+                    enqueue(s + k, full_mask(host_io), host_io)
+            graphs[key] = g
+        return graphs[key]
+
     def run_steps(s0, n, host_io=False):
-        """Exactly the work of layer-steps s0..s0+n-1: n + 3 graph replays
-        (the pipeline fills in the first three and drains in the last three)."""
+        """Exactly the work of layer-steps s0..s0+n-1 (the pipeline fills in
+        the first three graph steps and drains in the last three)."""
+        end = s0 + n + 3
+        full = full_mask(host_io)
         with torch.cuda.stream(compute):
-            for s in range(s0, s0 + n + 3):
-                graph_for(s, active_of(s, s0, n), host_io).replay()
+            s = s0
+            while s < end:
+                if s + n_inst <= end and all(active_of(s + k, s0, n, host_io) == full
+                                             for k in range(n_inst)):
+                    chunk_graph(s, host_io).replay()
+                    s += n_inst
+                else:
+                    graph_for(s, active_of(s, s0, n, host_io), host_io).replay()
+                    s += 1
 
     # capture every graph the long runs below need, outside the timed regions
-    long_masks = {active_of(s, 100, 50) for s in range(100, 153)}
-    for s in range(period):
-        for m in long_masks:
-            graph_for(s, m, False)
-            if not args.no_e2e:
-                graph_for(s, m, True)
+    for io in ((False,) if args.no_e2e else (False, True)):
+        masks = {active_of(s, 100, 50, io) for s in range(100, 153)}
+        for s in range(period):
+            for m in masks:
+                graph_for(s, m, io)
+            chunk_graph(s, io)
     torch.cuda.synchronize()
 
     if args.profile_steps:

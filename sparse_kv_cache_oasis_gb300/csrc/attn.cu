@@ -300,8 +300,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(
     }
     const int j = __shfl_sync(0xffffffffu, rj, st);
     const int blk = __shfl_sync(0xffffffffu, rb, st);
-    const int u = j / S;
-    while (cur_u < u) {  // units of this range before u are complete (possibly empty)
+    while (j >= (cur_u + 1) * S) {  // units of this range before j's are complete (possibly empty)
       flush();
       begin_unit(cur_u + 1);
     }
@@ -325,19 +324,21 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(
     const float mn_o = fmaxf(m_o, warp_max_xor_g(fmaxf(x1, x3)));
     const float mu_e = mn_e == -INFINITY ? 0.f : mn_e;
     const float mu_o = mn_o == -INFINITY ? 0.f : mn_o;
-    const float al_e = exp2f(m_e - mu_e), al_o = exp2f(m_o - mu_o);
-    const float p0 = exp2f(x0 - mu_e), p2 = exp2f(x2 - mu_e);
-    const float p1 = exp2f(x1 - mu_o), p3 = exp2f(x3 - mu_o);
+    const float al_e = ex2_approx(m_e - mu_e), al_o = ex2_approx(m_o - mu_o);
+    const float p0 = ex2_approx(x0 - mu_e), p2 = ex2_approx(x2 - mu_e);
+    const float p1 = ex2_approx(x1 - mu_o), p3 = ex2_approx(x3 - mu_o);
     l_e = l_e * al_e + p0 + p2;
     l_o = l_o * al_o + p1 + p3;
     m_e = mn_e;
     m_o = mn_o;
+    if (__any_sync(0xffffffffu, al_e != 1.f || al_o != 1.f)) {  // a running max moved
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      o[mt][0] *= al_e;
-      o[mt][1] *= al_o;
-      o[mt][2] *= al_e;
-      o[mt][3] *= al_o;
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= al_e;
+        o[mt][1] *= al_o;
+        o[mt][2] *= al_e;
+        o[mt][3] *= al_o;
+      }
     }
     const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));  // tokens 0-7
     const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));  // tokens 8-15

@@ -143,10 +143,12 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(
   const int tpw = t_hi - t_lo > warp ? (t_hi - t_lo - warp + kScoreWarps - 1) / kScoreWarps : 0;
 
   // copies tile i of this warp into stage i % kScoreStages (one commit group per call)
+  int u_iss = ua;  // unit of the last tile issued (tiles only move forward)
   auto issue = [&](int i) {
     if (i < tpw) {
       const int tile = t_lo + warp + kScoreWarps * i;
-      const int u = tile / ntiles;
+      while (tile >= (u_iss + 1) * ntiles) ++u_iss;
+      const int u = u_iss;
       const int blk = (tile - u * ntiles) * 8 + g;
       const int st = i % kScoreStages;
       if (blk < NB) {
@@ -184,10 +186,12 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(
   }
   __syncthreads();
 
+  int u_use = ua;  // unit of the tile being scored
 #pragma unroll 1
   for (int i = 0; i < tpw; ++i) {
     const int tile = t_lo + warp + kScoreWarps * i;
-    const int u = tile / ntiles;
+    while (tile >= (u_use + 1) * ntiles) ++u_use;
+    const int u = u_use;
     issue(i + kScoreStages - 1);
     cp_async_wait<kScoreStages - 1>();  // tile i has landed (this lane's copies)
     const int st = i % kScoreStages;
