@@ -307,13 +307,27 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(
     const uint32_t kt = ring_s + st * kStageBytes;
     const uint32_t vt = kt + 2 * kHalfTileBytes;
 
-    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    // S^T in two independent accumulator chains (even / odd k-steps)
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sac2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t af[4];
+    for (int kk = 0; kk < 8; kk += 2) {
+      uint32_t af[4], ag[4];
       ldmatrix_x4(af, kt + (kk >> 2) * kHalfTileBytes + swz(k_row, 2 * (kk & 3) + k_hi));
+      ldmatrix_x4(ag, kt + ((kk + 1) >> 2) * kHalfTileBytes + swz(k_row, 2 * ((kk + 1) & 3) + k_hi));
       mma_bf16_16816(sacc, af, qf[kk][0], qf[kk][1]);
+      mma_bf16_16816(sac2, ag, qf[kk + 1][0], qf[kk + 1][1]);
     }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) sacc[r] += sac2[r];
+    // V^T fragments into registers: the stage is then free and is refilled
+    // before the softmax and the O update, one slot's compute earlier
+    uint32_t vf[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+      ldmatrix_x4_trans(vf[mt], vt + (mt >> 2) * kHalfTileBytes + swz(v_row, 2 * (mt & 3) + v_hi));
+    __syncwarp();
+    ++consumed;
+    if (!exhausted) try_issue();  // refills the stage just read
     // tokens at or beyond the context length take no part
     const int tok0 = blk * kBlockSize + g;
     const float x0 = tok0 < ctx ? sacc[0] * scale_log2 : -INFINITY;
@@ -343,14 +357,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(
     const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));  // tokens 0-7
     const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));  // tokens 8-15
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      uint32_t af[4];
-      ldmatrix_x4_trans(af, vt + (mt >> 2) * kHalfTileBytes + swz(v_row, 2 * (mt & 3) + v_hi));
-      mma_bf16_16816(o[mt], af, pb0, pb1);
-    }
-    __syncwarp();
-    ++consumed;
-    if (!exhausted) try_issue();  // refills the stage just consumed
+    for (int mt = 0; mt < 8; ++mt) mma_bf16_16816(o[mt], vf[mt], pb0, pb1);
   }
   if (!ok) {
     if (lane == 0) set_error(err, OASIS_DEVERR_WAIT_TIMEOUT);

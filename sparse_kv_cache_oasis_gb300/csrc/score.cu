@@ -23,22 +23,26 @@
 // barrier.  The contraction index is permuted so that thread (g, t) of a warp
 // loads 16 contiguous bytes of block g: dims 16p+4t..16p+4t+3 serve k-steps
 // 2p and 2p+1 (A uses the same permutation, so the dot products are unchanged).
+// Each lane keeps its A fragments of the current unit in registers as the
+// queries' own bf16 pairs (a bf16 value is a tf32 value with zero low bits, so
+// unpacking is a shift or a mask); only the summaries pass through shared
+// memory, which halves the kernel's shared-memory traffic against staging the
+// queries there, and leaves the SM's shared-memory bandwidth to the attention
+// kernel running beside it.
 // Balance: the tiles of 8 consecutive blocks of all (request, KV head) units
 // form one list of T tiles; CTA c (one per SM) takes the contiguous range
-// [c*Rt, (c+1)*Rt) and its warps take every 8th tile of it, so every SM
-// streams the same number of bytes whatever NB and the unit count, and one
-// CTA per SM leaves room for the attention kernel's CTA beside it.  A range
-// meets at most kMaxUnits units (Rt is capped so); their query fragments are
-// staged in shared memory once per CTA.
+// [c*Rt, (c+1)*Rt) and each warp a contiguous eighth of it, so every SM
+// streams the same number of bytes whatever NB and the unit count, a warp
+// reloads its query fragments only where its tiles cross into the next unit,
+// and one CTA per SM leaves room for the attention kernel's CTA beside it.
 #include "common.cuh"
 #include "launch.h"
 
 namespace oasis {
 
-constexpr int kScoreThreads = 256;
+constexpr int kScoreThreads = 192;
 constexpr int kScoreWarps = kScoreThreads / 32;
 constexpr int kScoreStages = 3;  // tiles of 8 blocks in flight per warp (4 KiB each)
-constexpr int kMaxUnits = 2;     // units whose queries one CTA stages
 constexpr int kMinTilesPerCta = 16;
 
 // 16-byte asynchronous global->shared copy (bypasses L1) and its group fences.
@@ -55,9 +59,16 @@ __device__ __forceinline__ void cp_async_wait() {
 
 constexpr uint32_t kTf32Mask = 0xFFFFE000u;  // sign, exponent, 10 mantissa bits
 
+// Words per (16-row tile, k-step pair) of a lane's A fragments: the four
+// bf16-pair words they come in, unpacked at each use.  (Keeping them unpacked
+// saves ~64 instructions per tile but needs ~30 more registers per thread,
+// and the kernel must leave room in each SM sub-partition's register file for
+// the attention and top-K kernels that run beside it.)
+__host__ __device__ constexpr int frag_words(int) { return 4; }
+
 // Scores of 8 blocks (one tile) from their summaries in v; writes them out.
 template <int MT>
-__device__ __forceinline__ void score_tile(const float4 (&v)[8], const float4* sQ, int lane, int g,
+__device__ __forceinline__ void score_tile(const float4 (&v)[8], const uint32_t (&wq)[MT][8][frag_words(MT)], int lane, int g,
                                            int t, int M, int n0, int NB, int64_t out_off,
                                            float* out) {
   // four independent accumulator chains (hi/lo x even/odd k-step) keep the
@@ -77,12 +88,11 @@ __device__ __forceinline__ void score_tile(const float4 (&v)[8], const float4* s
     const uint32_t lw = __float_as_uint(v[p].w - __uint_as_float(hw));
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-      const float4 qa = sQ[((mt * 8 + p) * 2 + 0) * 32 + lane];
-      const float4 qb = sQ[((mt * 8 + p) * 2 + 1) * 32 + lane];
-      const uint32_t a0 = __float_as_uint(qa.x), a1 = __float_as_uint(qb.x);
-      const uint32_t a2 = __float_as_uint(qa.y), a3 = __float_as_uint(qb.y);
-      const uint32_t c0 = __float_as_uint(qa.z), c1 = __float_as_uint(qb.z);
-      const uint32_t c2 = __float_as_uint(qa.w), c3 = __float_as_uint(qb.w);
+      // rows g and g+8, dims 16p+4t..+3 as bf16 pairs -> tf32 bit patterns
+      const uint32_t a0 = wq[mt][p][0] << 16, a1 = wq[mt][p][2] << 16;
+      const uint32_t a2 = wq[mt][p][0] & 0xFFFF0000u, a3 = wq[mt][p][2] & 0xFFFF0000u;
+      const uint32_t c0 = wq[mt][p][1] << 16, c1 = wq[mt][p][3] << 16;
+      const uint32_t c2 = wq[mt][p][1] & 0xFFFF0000u, c3 = wq[mt][p][3] & 0xFFFF0000u;
       mma_tf32_1688(acc[mt], a0, a1, a2, a3, hx, hy);   // k-step 2p, hi
       mma_tf32_1688(acc1[mt], a0, a1, a2, a3, lx, ly);  // k-step 2p, lo
       mma_tf32_1688(acc2[mt], c0, c1, c2, c3, hz, hw);  // k-step 2p+1, hi
@@ -125,28 +135,27 @@ template <int MT>
 __global__ void __launch_bounds__(kScoreThreads) score_kernel(
     const uint16_t* __restrict__ q_draft, const float* __restrict__ summ,
     float* __restrict__ scores, int L, int Hq, int Hkv, int G, int NB, int T, int Rt) {
-  // shared memory: A fragments [unit][mt][p][half][lane] for the units of the
-  // range, then one ring per warp of kScoreStages tiles, each [p][lane] float4
-  // (a lane reads back what it copied)
+  // shared memory: one ring per warp of kScoreStages tiles, each [p][lane]
+  // float4 (a lane reads back what it copied)
   extern __shared__ float4 smem4[];
-  float4* sQ = smem4;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
-  float4* ring = smem4 + kMaxUnits * MT * 8 * 2 * 32 + warp * kScoreStages * 8 * 32;
+  float4* ring = smem4 + warp * kScoreStages * 8 * 32;
   const uint32_t ring_s = smem_u32(ring);
   const int M = L * G;
   const int ntiles = (NB + 7) >> 3;
   const int t_lo = blockIdx.x * Rt;
   const int t_hi = t_lo + Rt < T ? t_lo + Rt : T;
-  const int ua = t_lo / ntiles, ub = (t_hi - 1) / ntiles;  // ub - ua < kMaxUnits
-  // this warp's tiles: t_lo + warp + kScoreWarps * i
-  const int tpw = t_hi - t_lo > warp ? (t_hi - t_lo - warp + kScoreWarps - 1) / kScoreWarps : 0;
+  // this warp's tiles: the contiguous [w_lo, w_lo + tpw)
+  const int qw = (t_hi - t_lo + kScoreWarps - 1) / kScoreWarps;
+  const int w_lo = t_lo + warp * qw < t_hi ? t_lo + warp * qw : t_hi;
+  const int tpw = w_lo + qw < t_hi ? qw : t_hi - w_lo;
 
+  int u_iss = w_lo / ntiles;  // unit of the last tile issued (tiles only move forward)
   // copies tile i of this warp into stage i % kScoreStages (one commit group per call)
-  int u_iss = ua;  // unit of the last tile issued (tiles only move forward)
   auto issue = [&](int i) {
     if (i < tpw) {
-      const int tile = t_lo + warp + kScoreWarps * i;
+      const int tile = w_lo + i;
       while (tile >= (u_iss + 1) * ntiles) ++u_iss;
       const int u = u_iss;
       const int blk = (tile - u * ntiles) * 8 + g;
@@ -167,31 +176,38 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(
 #pragma unroll
   for (int i = 0; i < kScoreStages - 1; ++i) issue(i);
 
-  const int per_unit = MT * 8 * 2 * 32;
-  for (int idx = tid; idx < (ub - ua + 1) * per_unit; idx += kScoreThreads) {
-    const int us = idx / per_unit, r = idx - us * per_unit;
-    const int ln = r & 31, half = (r >> 5) & 1, p = (r >> 6) & 7, mt = r >> 9;
-    const int row = 16 * mt + (ln >> 2) + 8 * half;
-    const int col = 16 * p + 4 * (ln & 3);
-    const int u = ua + us, b = u / Hkv, h = u - b * Hkv;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row < M) {
-      const int l = row / G, gq = row - l * G;
-      const uint2 w = *reinterpret_cast<const uint2*>(
-          q_draft + ((static_cast<int64_t>(b) * L + l) * Hq + h * G + gq) * kHeadDim + col);
-      v = make_float4(bf16lo_to_f32(w.x), bf16hi_to_f32(w.x), bf16lo_to_f32(w.y),
-                      bf16hi_to_f32(w.y));
+  // A fragments of unit u: rows 16mt+g (+8), dims 16p+4t..+3, as bf16 pairs
+  // (rows >= L*G are padding and stay zero)
+  uint32_t wq[MT][8][frag_words(MT)];
+  auto load_q = [&](int u) {
+    const int b = u / Hkv, h = u - b * Hkv;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int row = 16 * mt + g + 8 * half;
+        const int l = row / G, gq = row - l * G;
+        const uint2* src = reinterpret_cast<const uint2*>(
+            q_draft + ((static_cast<int64_t>(b) * L + l) * Hq + h * G + gq) * kHeadDim + 4 * t);
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          const uint2 w = row < M ? __ldg(src + 4 * p) : make_uint2(0u, 0u);
+          wq[mt][p][2 * half] = w.x;
+          wq[mt][p][2 * half + 1] = w.y;
+        }
+      }
     }
-    sQ[idx] = v;
-  }
-  __syncthreads();
-
-  int u_use = ua;  // unit of the tile being scored
+  };
+  int u_use = -1;  // unit whose fragments are loaded
 #pragma unroll 1
   for (int i = 0; i < tpw; ++i) {
-    const int tile = t_lo + warp + kScoreWarps * i;
-    while (tile >= (u_use + 1) * ntiles) ++u_use;
-    const int u = u_use;
+    const int tile = w_lo + i;
+    int u = u_use < 0 ? tile / ntiles : u_use;
+    while (tile >= (u + 1) * ntiles) ++u;
+    if (u != u_use) {
+      load_q(u);
+      u_use = u;
+    }
     issue(i + kScoreStages - 1);
     cp_async_wait<kScoreStages - 1>();  // tile i has landed (this lane's copies)
     const int st = i % kScoreStages;
@@ -199,31 +215,26 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(
 #pragma unroll
     for (int p = 0; p < 8; ++p) v[p] = ring[(st * 8 + p) * 32 + lane];
     const int64_t out_off = static_cast<int64_t>(u) * NB;
-    score_tile<MT>(v, sQ + (u - ua) * per_unit, lane, g, t, M, (tile - u * ntiles) * 8, NB,
-                   out_off, scores + out_off);
+    score_tile<MT>(v, wq, lane, g, t, M, (tile - u * ntiles) * 8, NB, out_off, scores + out_off);
   }
   cp_async_wait<0>();
 }
 
-static size_t score_smem_bytes(int mt) {
-  return sizeof(float4) * (static_cast<size_t>(kMaxUnits) * mt * 8 * 2 * 32 +
-                           kScoreWarps * kScoreStages * 8 * 32);
+static size_t score_smem_bytes(int) {
+  return sizeof(float4) * static_cast<size_t>(kScoreWarps) * kScoreStages * 8 * 32;
 }
 
 template <int MT>
 static cudaError_t launch_mt(const Shape& s, const uint16_t* q_draft, const float* summ,
                              float* scores, cudaStream_t st, const DeviceInfo& di) {
-  // one CTA per SM over equal contiguous tile ranges, each range meeting at
-  // most kMaxUnits units
+  // one CTA per SM over equal contiguous tile ranges
   const int ntiles = (s.NB + 7) / 8;
   const int64_t T = static_cast<int64_t>(s.units()) * ntiles;
   int64_t C = di.sm_count > 0 ? di.sm_count : 148;
   const int64_t cap = (T + kMinTilesPerCta - 1) / kMinTilesPerCta;
   if (C > cap) C = cap;
   if (C < 1) C = 1;
-  int64_t Rt = (T + C - 1) / C;
-  const int64_t rmax = static_cast<int64_t>(kMaxUnits - 1) * ntiles + 1;
-  if (Rt > rmax) Rt = rmax;
+  const int64_t Rt = (T + C - 1) / C;
   const int64_t grid = (T + Rt - 1) / Rt;
   score_kernel<MT><<<static_cast<unsigned>(grid), kScoreThreads, score_smem_bytes(MT), st>>>(
       q_draft, summ, scores, s.L, s.Hq, s.Hkv, s.G, s.NB, static_cast<int>(T), static_cast<int>(Rt));
