@@ -46,6 +46,8 @@ oasis_status_t device_info(DeviceInfo* out) {
     di.err = static_cast<uint32_t*>(p);
     if (attn_configure(dev) != cudaSuccess) return OASIS_ERR_CUDA;
     if (score_configure() != cudaSuccess) return OASIS_ERR_CUDA;
+    if (pred_configure() != cudaSuccess) return OASIS_ERR_CUDA;
+    if (fetch_configure() != cudaSuccess) return OASIS_ERR_CUDA;
     di.score_ctas_per_sm = score_ctas_per_sm();
     di.attn_ctas_per_sm = attn_ctas_per_sm();
     d.info = di;

@@ -539,8 +539,12 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(
 }
 
 cudaError_t attn_configure(int) {
-  return cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kAttnSmem));
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kAttnSmem));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  return e;
 }
 
 int attn_ctas_per_sm() {

@@ -57,6 +57,13 @@ __global__ void __launch_bounds__(kFetchThreads) fetch_kernel(
   }
 }
 
+// Largest shared-memory carve-out (the transfer shares SMs with the attention
+// and scoring kernels of the step).
+cudaError_t fetch_configure() {
+  return cudaFuncSetAttribute(fetch_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
+}
+
 cudaError_t launch_fetch_blocks(const Shape& s, const uint16_t* host_k, const uint16_t* host_v,
                                 const int32_t* fetch_block, const int32_t* fetch_slot,
                                 const int32_t* n_fetch, uint16_t* pool_k, uint16_t* pool_v,

@@ -61,5 +61,7 @@ cudaError_t launch_sparse_decode_attn(const Shape& s, const uint16_t* q,
                                       cudaStream_t st, const DeviceInfo& di);
 int score_ctas_per_sm();
 cudaError_t score_configure();  // one-time function attributes
+cudaError_t pred_configure();   // one-time function attributes (top-K / plan kernels)
+cudaError_t fetch_configure();  // one-time function attributes
 
 }  // namespace oasis

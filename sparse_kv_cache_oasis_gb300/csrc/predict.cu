@@ -463,6 +463,29 @@ static PredLayout pred_layout(const Shape& s) {
   return lay;
 }
 
+// Largest shared-memory carve-out for the top-K / plan kernels: they run on
+// SMs that also host the attention and scoring kernels of the step.
+template <int N>
+static cudaError_t pred_configure_n() {
+  const int c = cudaSharedmemCarveoutMaxShared;
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel<N>, cudaFuncAttributePreferredSharedMemoryCarveout, c);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(topk_plan_kernel<N>, cudaFuncAttributePreferredSharedMemoryCarveout, c);
+  return e;
+}
+
+cudaError_t pred_configure() {
+  cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess) e = pred_configure_n<1>();
+  if (e == cudaSuccess) e = pred_configure_n<2>();
+  if (e == cudaSuccess) e = pred_configure_n<4>();
+  if (e == cudaSuccess) e = pred_configure_n<8>();
+  if (e == cudaSuccess) e = pred_configure_n<16>();
+  if (e == cudaSuccess) e = pred_configure_n<32>();
+  return e;
+}
+
 #define OASIS_ITEMS_SWITCH(items, CALL) \
   do {                                  \
     if ((items) <= 1) CALL(1);          \

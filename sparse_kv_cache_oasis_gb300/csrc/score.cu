@@ -253,12 +253,21 @@ cudaError_t launch_score_blocks(const Shape& s, const uint16_t* q_draft, const f
   }
 }
 
+template <int MT>
+static cudaError_t score_configure_mt() {
+  cudaError_t e = cudaFuncSetAttribute(score_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(score_smem_bytes(MT)));
+  if (e == cudaSuccess)  // largest carve-out: the step's other kernels share the SM
+    e = cudaFuncSetAttribute(score_kernel<MT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  return e;
+}
+
 cudaError_t score_configure() {
-  cudaError_t e = cudaSuccess;
-  e = cudaFuncSetAttribute(score_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)score_smem_bytes(1));
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(score_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)score_smem_bytes(2));
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(score_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)score_smem_bytes(3));
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(score_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)score_smem_bytes(4));
+  cudaError_t e = score_configure_mt<1>();
+  if (e == cudaSuccess) e = score_configure_mt<2>();
+  if (e == cudaSuccess) e = score_configure_mt<3>();
+  if (e == cudaSuccess) e = score_configure_mt<4>();
   return e;
 }
 
