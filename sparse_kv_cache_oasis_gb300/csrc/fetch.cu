@@ -12,7 +12,8 @@
 // link requests in flight: the transfer runs beside the HBM-bound attention
 // and scoring kernels, and an unbounded burst of long-latency host reads
 // slows their streams more than it speeds the transfer (measured on the 32K /
-// 2K-budget Llama layer step: 32 CTAs gave the shortest step).
+// 2K-budget Llama layer step, µs per step for 48/64/96/128/192/448 CTAs:
+// 33.5/32.6/32.6/33.4/38.0/44.0).
 #include "common.cuh"
 #include "launch.h"
 
@@ -21,7 +22,7 @@ namespace oasis {
 constexpr int kFetchThreads = 128;
 constexpr int kVecPerBlock = kBlockSize * kHeadDim * 2 / 16;  // 256 int4 per K (or V) block
 constexpr int kVecPerThread = kVecPerBlock / kFetchThreads;   // 2
-constexpr int kFetchCtas = 32;  // CTAs of the grid-stride gather (bounds the link requests in flight)
+constexpr int kFetchCtas = 64;  // CTAs of the grid-stride gather (bounds the link requests in flight)
 
 __global__ void __launch_bounds__(kFetchThreads) fetch_kernel(
     const int4* __restrict__ host_k, const int4* __restrict__ host_v,
