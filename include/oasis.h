@@ -10,6 +10,7 @@
  * ([OasisKV] Fig. 7 left, Fig. 9).  Once per layer and decode step:
  *
  *   oasis_sparse_decode_attn   attention over the working set      (Fig. 7 right)
+ *   oasis_attend_and_score     attention of one layer + scoring of another in one launch (Fig. 8)
  *   oasis_score_blocks         draft queries scan compressed keys  (Fig. 7 right)
  *   oasis_select_topk          top-K blocks per KV head            (diagram step 2)
  *   oasis_plan_fetch           diff vs. working set, capped LRU    (diagram step 3, Tab. 2)
@@ -192,11 +193,10 @@ oasis_status_t oasis_fetch_blocks(const oasis_config_t* cfg, const uint16_t* hos
  * (block_of_slot >= 0, block*bs + t < ctx_len[b]) of scale * q.k, times v.
  * One pass, online softmax, fp32 accumulation, bf16 output; a head with no
  * visible token outputs zeros.  ctx_len is [B] int32 or NULL (no mask).
- * `workspace` is caller-owned device scratch of at least
- * oasis_attn_workspace_bytes(cfg) bytes, 256-byte aligned, zero-filled once
- * before its first use; every call leaves it ready for the next one.  Calls
- * that share a workspace must not overlap on the GPU.  q, pools and out
- * 16-byte aligned; scale > 0. */
+ * The kernel keeps all of its scratch in shared memory (each unit's CTAs merge
+ * through distributed shared memory); `workspace` is accepted for
+ * compatibility and never touched: at least oasis_attn_workspace_bytes(cfg)
+ * bytes, 256-byte aligned.  q, pools and out 16-byte aligned; scale > 0. */
 oasis_status_t oasis_sparse_decode_attn(const oasis_config_t* cfg, const uint16_t* q,
                                         const uint16_t* pool_k, const uint16_t* pool_v,
                                         const int32_t* block_of_slot, const int32_t* ctx_len,
@@ -212,7 +212,7 @@ size_t oasis_attn_workspace_bytes(const oasis_config_t* cfg);
  * where a cudaMalloc (which may synchronize) is not acceptable.  The method's
  * pages have no counterpart: this is a deployment convenience.
  * Same arguments and result as oasis_sparse_decode_attn, without the
- * workspace: the scratch is a fixed 8 MiB array in device memory that every
+ * workspace: its scratch is a fixed 8 MiB array in device memory that every
  * GPU that loads this library holds until the process exits.  The caller
  * still owns q, the pools, block_of_slot, ctx_len and out.  Nothing is
  * allocated: no cudaMalloc, no cudaFree, no allocating library call.
@@ -220,15 +220,27 @@ size_t oasis_attn_workspace_bytes(const oasis_config_t* cfg);
  * oasis_attn_workspace_bytes) return OASIS_ERR_UNSUPPORTED and launch
  * nothing.  The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  Every call clears the array's arrival counters on
- * `stream` before its kernel; the rest of the array keeps what the last call
- * left.  All calls on a device share the one array, so calls that overlap on
- * the GPU (different streams without ordering) race and give wrong results. */
+ * any stream capture.  The current attention kernel keeps all its scratch in
+ * shared memory, so the array is passed but not written, and calls on
+ * different streams do not interfere. */
 oasis_status_t oasis_sparse_decode_attn_static(const oasis_config_t* cfg, const uint16_t* q,
                                                const uint16_t* pool_k, const uint16_t* pool_v,
                                                const int32_t* block_of_slot,
                                                const int32_t* ctx_len, float scale,
                                                uint16_t* out, void* stream);
+
+/* The attention of one layer and the look-ahead scoring of another, with the
+ * same configuration, in one launch: exactly oasis_sparse_decode_attn(cfg, q,
+ * pool_k, pool_v, block_of_slot, ctx_len, scale, out) and
+ * oasis_score_blocks(cfg, q_draft, summ, scores), bit for bit, with the SMs
+ * shared between the two by construction ([OasisKV] Fig. 8: a layer's
+ * prediction runs in the background of the following layers' compute).  The
+ * two must not share output memory.  Same argument rules as the two calls. */
+oasis_status_t oasis_attend_and_score(const oasis_config_t* cfg, const uint16_t* q,
+                                      const uint16_t* pool_k, const uint16_t* pool_v,
+                                      const int32_t* block_of_slot, const int32_t* ctx_len,
+                                      float scale, uint16_t* out, const uint16_t* q_draft,
+                                      const float* summ, float* scores, void* stream);
 
 /* Pins and maps `bytes` of existing host memory at `host` (cudaHostRegister,
  * mapped) and returns in *dev_ptr the address kernels use to read it: the

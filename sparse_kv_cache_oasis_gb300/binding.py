@@ -64,6 +64,8 @@ _SIGS = {
     "oasis_attn_workspace_bytes": (C.c_size_t, [C.POINTER(OasisConfig)]),
     "oasis_sparse_decode_attn_static": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P, _P, _P,
                                                   C.c_float, _P, _P]),
+    "oasis_attend_and_score": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P, _P, _P, C.c_float,
+                                         _P, _P, _P, _P, _P]),
     "oasis_host_register": (C.c_int, [_P, C.c_size_t, C.POINTER(C.c_void_p)]),
     "oasis_host_unregister": (C.c_int, [_P]),
     "oasis_device_errors": (C.c_int, [C.POINTER(C.c_uint32), C.c_int32]),
@@ -289,6 +291,24 @@ def oasis_sparse_decode_attn_static(cfg, q, pool_k, pool_v, block_of_slot, ctx_l
         _ptr(pool_v, torch.bfloat16, (B, H, S, bs, D), "pool_v"),
         _ptr(block_of_slot, torch.int32, (B, H, S), "block_of_slot"), cl, float(scale),
         _ptr(out, torch.bfloat16, (B, Hq, D), "out"), _stream(stream)))
+
+
+def oasis_attend_and_score(cfg, q, pool_k, pool_v, block_of_slot, ctx_len, scale, out,
+                           q_draft, summ, scores, stream=None) -> None:
+    """oasis_sparse_decode_attn(q, pools, ...) and oasis_score_blocks(q_draft,
+    summ, scores) -- usually of two different layers -- in one launch."""
+    c = OasisConfig.make(cfg)
+    B, H, Hq, NB, bs, D, S = _dims(c)
+    cl = None if ctx_len is None else _ptr(ctx_len, torch.int32, (B,), "ctx_len")
+    _check("oasis_attend_and_score", lib().oasis_attend_and_score(
+        C.byref(c), _ptr(q, torch.bfloat16, (B, Hq, D), "q"),
+        _ptr(pool_k, torch.bfloat16, (B, H, S, bs, D), "pool_k"),
+        _ptr(pool_v, torch.bfloat16, (B, H, S, bs, D), "pool_v"),
+        _ptr(block_of_slot, torch.int32, (B, H, S), "block_of_slot"), cl, float(scale),
+        _ptr(out, torch.bfloat16, (B, Hq, D), "out"),
+        _ptr(q_draft, torch.bfloat16, (B, c.lookahead, Hq, D), "q_draft"),
+        _ptr(summ, torch.float32, (B, H, NB, D), "summ"),
+        _ptr(scores, torch.float32, (B, H, NB), "scores"), _stream(stream)))
 
 
 def oasis_host_register(tensor: torch.Tensor) -> int:

@@ -59,6 +59,16 @@ cudaError_t launch_sparse_decode_attn(const Shape& s, const uint16_t* q,
                                       const int32_t* block_of_slot, const int32_t* ctx_len,
                                       float scale, uint16_t* out, void* workspace,
                                       cudaStream_t st, const DeviceInfo& di);
+int attn_split(const Shape& s, int sm_count);  // CTAs per unit (cluster size)
+
+// Attention of one layer and scoring of another in one launch (same shapes).
+cudaError_t fused_configure();  // one-time function attributes
+cudaError_t launch_attend_and_score(const Shape& s, const CUtensorMap& tm_k,
+                                    const CUtensorMap& tm_v, const uint16_t* q,
+                                    const int32_t* block_of_slot, const int32_t* ctx_len,
+                                    float scale, uint16_t* out, const uint16_t* q_draft,
+                                    const float* summ, float* scores, cudaStream_t st,
+                                    const DeviceInfo& di);
 int score_ctas_per_sm();
 cudaError_t score_configure();  // one-time function attributes
 cudaError_t pred_configure();   // one-time function attributes (top-K / plan kernels)
