@@ -70,6 +70,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest `value` over the ranks: the slowest replica sets the job's
+    time.  One all-reduce of one number (the replicas share no data)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, batch: int, ms_per_step: float) -> float:
+    """Decode tokens per second of the whole job: every rank decodes `batch`
+    sequences per layer-step (weak scaling)."""
+    return world * batch / (ms_per_step * 1e-3)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -228,6 +246,53 @@ def reference_arm(args):
                                        "layer-step, single-threaded C oracle, double accumulation"},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def cpu_baseline_all_cores(seconds: float):
+    """The same oracle, its independent (request, KV head) units spread over
+    all host cores: each unit keeps its own single-threaded oracle state and a
+    thread pool runs the units of a layer-step side by side (the C calls
+    release the interpreter lock)."""
+    from concurrent.futures import ThreadPoolExecutor
+    import oracle
+    wl = WORKLOAD
+    cores = os.cpu_count() or 1
+    cfg = wl.config()
+    qseq = W.query_sequence(wl, 0)
+    k, v = W.gen_kv(wl, 0, qseq)
+    sob, bos, lu = W.initial_resident(wl, 0)
+    pk, pv = W.initial_pool(wl, k, v, bos)
+    summ = oracle.build_summaries(cfg, k)
+    ucfg = oracle.unit_cfg(cfg)
+    G = wl.group
+    units = []
+    for u in range(wl.batch * wl.num_kv_heads):
+        b, h = divmod(u, wl.num_kv_heads)
+        sl = lambda a: np.ascontiguousarray(a[b:b + 1, h:h + 1])
+        units.append((b, h, oracle.Stepper(ucfg, sl(k), sl(v), sl(summ), sl(sob), sl(bos), sl(lu),
+                                           sl(pk), sl(pv))))
+    del k, v
+
+    def one(pool, t):
+        q, qd = W.step_queries(wl, qseq, t % wl.steps)
+        jobs = [pool.submit(st.step, t, np.ascontiguousarray(q[b:b + 1, h * G:(h + 1) * G]),
+                            np.ascontiguousarray(qd[b:b + 1, :, h * G:(h + 1) * G]))
+                for b, h, st in units]
+        for j in jobs:
+            j.result()
+
+    with ThreadPoolExecutor(max_workers=cores) as pool:
+        one(pool, 0)
+        n, t0 = 0, time.perf_counter()
+        while True:
+            one(pool, n + 1)
+            n += 1
+            dt = time.perf_counter() - t0
+            if dt >= seconds or n >= 500:
+                break
+    return {"value": wl.batch * n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} full layer-steps of {wl.name}, its 64 units spread over {cores} threads "
+                      "(one single-threaded C oracle per unit)"}
 
 
 def cpu_baseline(seconds: float):
@@ -496,13 +561,9 @@ def gpu_arm(args):
         dist.barrier()
     clk = clocks.stop()
     s += args.steps
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     ms_per_step = ms / args.steps
-    value = world * wl.batch / (ms_per_step * 1e-3)
+    value = job_throughput(world, wl.batch, ms_per_step)
 
     # ---- per-kernel timing: a CUDA graph of 8 launches of one kernel over the
     # layer copies (cold L2), bracketed by events on the launching stream
@@ -575,6 +636,11 @@ def gpu_arm(args):
     del hb, db
     t_roof = max(by["hbm"] / (peak * 1e9), by["link"] / (link_gbs * 1e9))
     step_frac = t_roof / (ms_per_step * 1e-3)
+    # the narrower forms: resident KV read by the attention and the fetched
+    # bytes only, as the slowest tier (max) and as the sum of the two tiers
+    kv_read = valid_avg * wl.block_size * wl.head_dim * 2 * 2
+    t_kv = kv_read / (peak * 1e9)
+    t_link = by["link"] / (link_gbs * 1e9)
 
     # ---- end to end: inputs copied in from pinned host, output read back, every step
     e2e = None
@@ -591,20 +657,17 @@ def gpu_arm(args):
         torch.cuda.synchronize()
         wall = time.perf_counter() - w0
         s += n_e2e
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            tt = torch.tensor([ems], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ems = float(tt.item())
+        ems = max_over_ranks(e0.elapsed_time(e1), world, dev)
         q_bytes = q_host[0][0].numel() * 2 + qd_host[0][0].numel() * 2
-        e2e = {"value": world * wl.batch / (ems / n_e2e * 1e-3), "unit": UNIT,
+        e2e = {"value": job_throughput(world, wl.batch, ems / n_e2e), "unit": UNIT,
                "h2d_bytes_per_step": q_bytes, "d2h_bytes_per_step": out_host[0].numel() * 2,
                "wall_s": wall}
 
     errs = ob.oasis_device_errors()
-    cpu = None
+    cpu = cpu_all = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_seconds)
+        cpu_all = cpu_baseline_all_cores(args.cpu_seconds)
 
     if rank == 0:
         line = {
@@ -626,12 +689,16 @@ def gpu_arm(args):
             "step_roofline": {"t_roof_us": t_roof * 1e6, "t_step_us": ms_per_step * 1e3,
                               "frac": step_frac, "hbm_bytes": by["hbm"], "link_bytes": by["link"],
                               "hbm_peak_gbs": peak, "link_peak_gbs": link_gbs,
-                              "fetched_blocks_per_step": n_fetch_avg},
+                              "fetched_blocks_per_step": n_fetch_avg,
+                              "kv_read_bytes": kv_read,
+                              "frac_kv_read_and_link_max": max(t_kv, t_link) / (ms_per_step * 1e-3),
+                              "frac_kv_read_plus_link_sum": (t_kv + t_link) / (ms_per_step * 1e-3)},
             "kernels_ms": mean_ms,
             "kernel_gbs": {k: by[k] / (mean_ms[k] * 1e-3) / 1e9 for k in kinds},
             "gpu_launches": args.steps * 4,
             "clocks": clk,
             "cpu_baseline": cpu,
+            "cpu_baseline_all_cores": cpu_all,
             "e2e": e2e,
             "device_errors": errs,
         }
