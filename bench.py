@@ -350,24 +350,28 @@ def gpu_arm(args):
     dev = torch.device("cuda", local)
 
     # ---- layer copies (set-up, untimed)
-    layers, qd_dev, q_dev, q_host, qd_host = [], [], [], [], []
+    layers, qd_dev, q_dev, q_host, qd_host, qq_host = [], [], [], [], [], []
     for i in range(n_inst):
         qseq = W.query_sequence(wl, i)
         k, v = W.gen_kv(wl, i, qseq)
         sob, bos, lu = W.initial_resident(wl, i)
         layers.append(LayerState(wl, bits_to_bf16(k), bits_to_bf16(v), sob, bos, lu, device=str(dev)))
         del k, v
-        qs, qds, hq, hqd = [], [], [], []
+        qs, qds, hq, hqd, hqq = [], [], [], [], []
         for t in range(QUERY_SETS):
             q, qd = W.step_queries(wl, qseq, t)
-            hq.append(bits_to_bf16(q).pin_memory())
-            hqd.append(bits_to_bf16(qd).pin_memory())
+            # a step's queries and draft queries sit in one pinned buffer: one copy per step
+            both = torch.cat([bits_to_bf16(q).flatten(), bits_to_bf16(qd).flatten()]).pin_memory()
+            hqq.append(both)
+            hq.append(both[:q.size].view(q.shape))
+            hqd.append(both[q.size:].view(qd.shape))
             qs.append(hq[-1].to(dev))
             qds.append(hqd[-1].to(dev))
         q_dev.append(qs)
         qd_dev.append(qds)
         q_host.append(hq)
         qd_host.append(hqd)
+        qq_host.append(hqq)
     torch.cuda.synchronize()
 
     compute = torch.cuda.Stream(device=dev)
@@ -377,8 +381,10 @@ def gpu_arm(args):
     h2d = torch.cuda.Stream(device=dev)
     d2h = torch.cuda.Stream(device=dev)
     out_host = [torch.empty_like(L.out, device="cpu").pin_memory() for L in layers]
-    q_in = [torch.empty_like(q_dev[i][0]) for i in range(n_inst)]
-    qd_in = [torch.empty_like(qd_dev[i][0]) for i in range(n_inst)]
+    qq_in = [torch.empty_like(qq_host[i][0], device=dev) for i in range(n_inst)]
+    nq = q_dev[0][0].numel()
+    q_in = [qq_in[i][:nq].view(q_dev[i][0].shape) for i in range(n_inst)]
+    qd_in = [qq_in[i][nq:].view(qd_dev[i][0].shape) for i in range(n_inst)]
 
     def qset(s):
         return s % n_inst, (s // n_inst) % QUERY_SETS
@@ -409,8 +415,7 @@ def gpu_arm(args):
         def copy_in(stream, step):
             i, qi = qset(step)
             with torch.cuda.stream(stream):
-                q_in[i].copy_(q_host[i][qi], non_blocking=True)
-                qd_in[i].copy_(qd_host[i][qi], non_blocking=True)
+                qq_in[i].copy_(qq_host[i][qi], non_blocking=True)
 
         if "h2d_now" in active:
             branch(h2d, lambda st: copy_in(st, s))
