@@ -16,7 +16,7 @@ namespace cg = cooperative_groups;
 
 constexpr int kAttnWarps = 4;
 constexpr int kAttnThreads = kAttnWarps * 32;
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kStageBytes = 2 * kBlockSize * kHeadDim * 2;  // K + V of one slot: 8 KiB
 constexpr int kHalfTileBytes = kBlockSize * 64 * 2;         // 16 rows x 128 B
 constexpr int kRingBytes = kStages * kStageBytes;

@@ -25,12 +25,11 @@ __device__ __forceinline__ void cp_async_wait() {
 
 constexpr uint32_t kTf32Mask = 0xFFFFE000u;  // sign, exponent, 10 mantissa bits
 
-// Words per (16-row tile, k-step pair) of a lane's A fragments: the four
-// bf16-pair words they come in, unpacked at each use.  (Keeping them unpacked
-// saves ~64 instructions per tile but needs ~30 more registers per thread,
-// and the kernel must leave room in each SM sub-partition's register file for
-// the attention and top-K kernels that run beside it.)
-__host__ __device__ constexpr int frag_words(int) { return 4; }
+// Words per (16-row tile, k-step pair) of a lane's A fragments: with one row
+// tile they are kept unpacked (eight tf32 bit patterns, 64 instructions per
+// tile fewer), with more as the four bf16-pair words they come in, unpacked at
+// each use (to bound the registers).
+__host__ __device__ constexpr int frag_words(int mt) { return mt == 1 ? 8 : 4; }
 
 // Scores of 8 blocks (one tile) from their summaries in v; writes them out.
 template <int MT>
@@ -54,11 +53,16 @@ __device__ __forceinline__ void score_tile(const float4 (&v)[8], const uint32_t 
     const uint32_t lw = __float_as_uint(v[p].w - __uint_as_float(hw));
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-      // rows g and g+8, dims 16p+4t..+3 as bf16 pairs -> tf32 bit patterns
-      const uint32_t a0 = wq[mt][p][0] << 16, a1 = wq[mt][p][2] << 16;
-      const uint32_t a2 = wq[mt][p][0] & 0xFFFF0000u, a3 = wq[mt][p][2] & 0xFFFF0000u;
-      const uint32_t c0 = wq[mt][p][1] << 16, c1 = wq[mt][p][3] << 16;
-      const uint32_t c2 = wq[mt][p][1] & 0xFFFF0000u, c3 = wq[mt][p][3] & 0xFFFF0000u;
+      uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+      if constexpr (MT == 1) {
+        a0 = wq[mt][p][0]; a1 = wq[mt][p][1]; a2 = wq[mt][p][2]; a3 = wq[mt][p][3];
+        c0 = wq[mt][p][4]; c1 = wq[mt][p][5]; c2 = wq[mt][p][6]; c3 = wq[mt][p][7];
+      } else {
+        a0 = wq[mt][p][0] << 16; a1 = wq[mt][p][2] << 16;
+        a2 = wq[mt][p][0] & 0xFFFF0000u; a3 = wq[mt][p][2] & 0xFFFF0000u;
+        c0 = wq[mt][p][1] << 16; c1 = wq[mt][p][3] << 16;
+        c2 = wq[mt][p][1] & 0xFFFF0000u; c3 = wq[mt][p][3] & 0xFFFF0000u;
+      }
       mma_tf32_1688(acc[mt], a0, a1, a2, a3, hx, hy);   // k-step 2p, hi
       mma_tf32_1688(acc1[mt], a0, a1, a2, a3, lx, ly);  // k-step 2p, lo
       mma_tf32_1688(acc2[mt], c0, c1, c2, c3, hz, hw);  // k-step 2p+1, hi
@@ -151,8 +155,15 @@ __device__ __forceinline__ void score_warp_range(const uint16_t* __restrict__ q_
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
           const uint2 w = row < M ? __ldg(src + 4 * p) : make_uint2(0u, 0u);
-          wq[mt][p][2 * half] = w.x;
-          wq[mt][p][2 * half + 1] = w.y;
+          if constexpr (MT == 1) {
+            wq[mt][p][half] = w.x << 16;
+            wq[mt][p][2 + half] = w.x & 0xFFFF0000u;
+            wq[mt][p][4 + half] = w.y << 16;
+            wq[mt][p][6 + half] = w.y & 0xFFFF0000u;
+          } else {
+            wq[mt][p][2 * half] = w.x;
+            wq[mt][p][2 * half + 1] = w.y;
+          }
         }
       }
     }
