@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="only run this many untimed graph steps (for ncu launch lists)")
+    ap.add_argument("--profile-joint", type=int, default=0,
+                    help="with --profile-steps: then this many joint-attention launches")
     return ap.parse_args()
 
 
@@ -110,8 +112,11 @@ def algorithmic_bytes(wl, n_fetch_blocks: float, valid_slots: float):
     plan = U * (wl.top_k * 4 + wl.slots * 4 * 4)        # ids, maps, LRU (read + write)
     fetch_hbm = n_fetch_blocks * blk
     link = n_fetch_blocks * blk
+    # joint attention: the same KV pass with the draft rows as queries and outputs too
+    rows_io = wl.batch * wl.num_q_heads * wl.head_dim * 2 * (1 + wl.lookahead)
+    joint = valid_slots * blk + 2 * rows_io + U * wl.slots * 4
     return dict(attn=attn, score=score, fused=attn + score, topk=topk, plan=plan, fetch=fetch_hbm,
-                hbm=attn + score + topk + plan + fetch_hbm, link=link)
+                hbm=attn + score + topk + plan + fetch_hbm, link=link, joint=joint)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -537,8 +542,11 @@ def gpu_arm(args):
 
     if args.profile_steps:
         run_steps(0, args.profile_steps)
+        for r in range(args.profile_joint):  # joint attention launches after the steps
+            layers[r % n_inst].attention_joint(q_dev[r % n_inst][0], qd_dev[r % n_inst][0], compute)
         torch.cuda.synchronize()
-        print(json.dumps({"profile_steps": args.profile_steps}), flush=True)
+        print(json.dumps({"profile_steps": args.profile_steps, "profile_joint": args.profile_joint}),
+              flush=True)
         return
 
     # ---- warm-up and timed region
@@ -590,9 +598,11 @@ def gpu_arm(args):
                 elif kind == "fused":
                     L.attention_and_score(q_dev[i][0], layers[(i + 1) % n_inst],
                                           qd_dev[(i + 1) % n_inst][0], compute)
+                elif kind == "joint":
+                    L.attention_joint(q_dev[i][0], qd_dev[i][0], compute)
         return g
 
-    kinds = ["attn", "score", "topk", "fused"]
+    kinds = ["attn", "score", "topk", "fused", "joint"]
     mean_ms = {}
     for kind in kinds:
         g = kernel_graph(kind)
@@ -702,6 +712,12 @@ def gpu_arm(args):
                               "kv_read_bytes": kv_read,
                               "frac_kv_read_and_link_max": max(t_kv, t_link) / (ms_per_step * 1e-3),
                               "frac_kv_read_plus_link_sum": (t_kv + t_link) / (ms_per_step * 1e-3)},
+            "joint_attention": {
+                "kernel": "attn_joint_kernel", "rows_per_unit": wl.group * (1 + wl.lookahead),
+                "ms_per_launch": mean_ms["joint"], "bytes_per_launch": by["joint"],
+                "achieved_gbs": by["joint"] / (mean_ms["joint"] * 1e-3) / 1e9,
+                "frac_of_measured_hbm": by["joint"] / (mean_ms["joint"] * 1e-3) / 1e9 / peak,
+                "vs_single_query_attention": mean_ms["joint"] / mean_ms["attn"]},
             "kernels_ms": mean_ms,
             "kernel_gbs": {k: by[k] / (mean_ms[k] * 1e-3) / 1e9 for k in kinds},
             "gpu_launches": args.steps * 4,

@@ -11,6 +11,7 @@
  *
  *   oasis_sparse_decode_attn   attention over the working set      (Fig. 7 right)
  *   oasis_attend_and_score     attention of one layer + scoring of another in one launch (Fig. 8)
+ *   oasis_sparse_decode_attn_joint  decoded + draft tokens in one pass of the working set (Fig. 7 right)
  *   oasis_score_blocks         draft queries scan compressed keys  (Fig. 7 right)
  *   oasis_select_topk          top-K blocks per KV head            (diagram step 2)
  *   oasis_plan_fetch           diff vs. working set, capped LRU    (diagram step 3, Tab. 2)
@@ -241,6 +242,28 @@ oasis_status_t oasis_attend_and_score(const oasis_config_t* cfg, const uint16_t*
                                       const int32_t* block_of_slot, const int32_t* ctx_len,
                                       float scale, uint16_t* out, const uint16_t* q_draft,
                                       const float* summ, float* scores, void* stream);
+
+/* Joint attention of the decoded token and the L draft tokens over the same
+ * working set, in one pass over its K and V ([OasisKV] Fig. 7 right: the
+ * attention kernel processes the normal and the draft queries together).
+ *   out[b, 0, n, :] = the oasis_sparse_decode_attn output for q[b, n, :]
+ *   out[b, l, n, :] = the same attention with q_draft[b, l-1, n, :] as the
+ *                     query, 1 <= l <= L
+ * with the same slots, context mask and scale for all 1 + L rows (the draft
+ * tokens' own keys are not in the cache).
+ *   q        [B][Hq][D]         bf16
+ *   q_draft  [B][L][Hq][D]      bf16
+ *   out      [B][1+L][Hq][D]    bf16 (written in full; every row of a unit
+ *                               whose slots are all empty or masked is 0)
+ * Pools, block_of_slot, ctx_len and scale as for oasis_sparse_decode_attn.
+ * Needs no workspace.  q, q_draft, pools and out 16-byte aligned; scale > 0.
+ * Any group size G: the G*(1+L) rows of a KV head are taken 24 at a time,
+ * and each further 24 rows stream the head's slots once more. */
+oasis_status_t oasis_sparse_decode_attn_joint(const oasis_config_t* cfg, const uint16_t* q,
+                                              const uint16_t* q_draft, const uint16_t* pool_k,
+                                              const uint16_t* pool_v, const int32_t* block_of_slot,
+                                              const int32_t* ctx_len, float scale, uint16_t* out,
+                                              void* stream);
 
 /* Pins and maps `bytes` of existing host memory at `host` (cudaHostRegister,
  * mapped) and returns in *dev_ptr the address kernels use to read it: the

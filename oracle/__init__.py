@@ -209,6 +209,22 @@ def sparse_decode_attn(cfg: dict, q, pool_k, pool_v, block_of_slot, ctx_len=None
     return out
 
 
+def sparse_decode_attn_joint(cfg: dict, q, q_draft, pool_k, pool_v, block_of_slot, ctx_len=None,
+                             scale: float | None = None) -> np.ndarray:
+    """Attention of the decoded token and of each draft token over the same
+    working set ([OasisKV] Fig. 7 right: the attention kernel takes the normal
+    and the draft queries together).  Reading: every one of the 1 + L query
+    rows sees the same resident slots under the same context mask, since the
+    draft tokens' own keys are not in the cache.  Output [B, 1+L, Hq, D]
+    fp32: row 0 from q, row l from q_draft[:, l-1]."""
+    B, H, Hq, NB, bs, D, S = _sizes(cfg)
+    L = cfg["lookahead"]
+    _check(q_draft, (B, L, Hq, D), "q_draft")
+    rows = [q] + [np.ascontiguousarray(q_draft[:, l]) for l in range(L)]
+    return np.stack([sparse_decode_attn(cfg, r, pool_k, pool_v, block_of_slot, ctx_len, scale)
+                     for r in rows], axis=1)
+
+
 def dense_decode_attn(cfg: dict, q, k, v, ctx_len=None, scale: float | None = None) -> np.ndarray:
     B, H, Hq, NB, bs, D, S = _sizes(cfg)
     _check(q, (B, Hq, D), "q")

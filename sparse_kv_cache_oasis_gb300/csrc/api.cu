@@ -49,6 +49,7 @@ oasis_status_t device_info(DeviceInfo* out) {
     if (pred_configure() != cudaSuccess) return OASIS_ERR_CUDA;
     if (fetch_configure() != cudaSuccess) return OASIS_ERR_CUDA;
     if (fused_configure() != cudaSuccess) return OASIS_ERR_CUDA;
+    if (joint_configure() != cudaSuccess) return OASIS_ERR_CUDA;
     di.score_ctas_per_sm = score_ctas_per_sm();
     di.attn_ctas_per_sm = attn_ctas_per_sm();
     d.info = di;
@@ -332,6 +333,31 @@ oasis_status_t oasis_sparse_decode_attn(const oasis_config_t* cfg, const uint16_
   if ((st = encode_pool(&tv, pool_v, s)) != OASIS_OK) return st;
   return from_cuda(launch_sparse_decode_attn(s, q, tk, tv, block_of_slot, ctx_len, scale, out,
                                              workspace, static_cast<cudaStream_t>(stream), di));
+}
+
+oasis_status_t oasis_sparse_decode_attn_joint(const oasis_config_t* cfg, const uint16_t* q,
+                                              const uint16_t* q_draft, const uint16_t* pool_k,
+                                              const uint16_t* pool_v, const int32_t* block_of_slot,
+                                              const int32_t* ctx_len, float scale, uint16_t* out,
+                                              void* stream) {
+  Shape s;
+  oasis_status_t st = make_shape(cfg, &s);
+  if (st != OASIS_OK) return st;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return OASIS_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(q_draft, 16) || !aligned(pool_k, 16) || !aligned(pool_v, 16) ||
+      !aligned(out, 16) || !aligned(block_of_slot, 4))
+    return OASIS_ERR_INVALID_ARG;
+  if (ctx_len && !aligned(ctx_len, 4)) return OASIS_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != OASIS_OK) return st;
+  const JointSplit j = joint_split(s, di.sm_count);
+  if (static_cast<int64_t>(s.units()) * j.groups * j.P > 0x7fffffff) return OASIS_ERR_UNSUPPORTED;
+  CUtensorMap tk, tv;
+  if ((st = encode_pool(&tk, pool_k, s)) != OASIS_OK) return st;
+  if ((st = encode_pool(&tv, pool_v, s)) != OASIS_OK) return st;
+  return from_cuda(launch_sparse_decode_attn_joint(s, q, q_draft, tk, tv, block_of_slot, ctx_len,
+                                                   scale, out, static_cast<cudaStream_t>(stream),
+                                                   di));
 }
 
 oasis_status_t oasis_attend_and_score(const oasis_config_t* cfg, const uint16_t* q,

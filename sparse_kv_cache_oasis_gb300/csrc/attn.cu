@@ -70,8 +70,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int u = blockIdx.x / P, r = blockIdx.x - u * P;  // unit, rank in its cluster
-  attn_cta(&tm_k, &tm_v, q, block_of_slot, ctx_len, scale_log2, out, Hq, Hkv, G, S, NB, P, err, smem,
-           u, r, threadIdx.x >> 5, threadIdx.x & 31, [] { __syncthreads(); });
+  const int b = u / Hkv, h = u - b * Hkv;
+  const GroupRows rows{q, out, (static_cast<int64_t>(b) * Hq + h * G) * kHeadDim};
+  attn_cta<1>(&tm_k, &tm_v, rows, G, block_of_slot, ctx_len, scale_log2, Hkv, S, NB, P, err, smem,
+              u, r, threadIdx.x >> 5, threadIdx.x & 31, [] { __syncthreads(); });
 }
 
 cudaError_t attn_configure(int) {

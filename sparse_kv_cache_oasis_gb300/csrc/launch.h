@@ -61,6 +61,20 @@ cudaError_t launch_sparse_decode_attn(const Shape& s, const uint16_t* q,
                                       cudaStream_t st, const DeviceInfo& di);
 int attn_split(const Shape& s, int sm_count);  // CTAs per unit (cluster size)
 
+// Joint attention of the decoded and the draft tokens: row tiles per CTA,
+// row groups per unit and CTAs per (unit, row group).
+struct JointSplit {
+  int nt, groups, P;
+};
+JointSplit joint_split(const Shape& s, int sm_count);
+cudaError_t joint_configure();  // one-time function attributes
+cudaError_t launch_sparse_decode_attn_joint(const Shape& s, const uint16_t* q,
+                                            const uint16_t* q_draft, const CUtensorMap& tm_k,
+                                            const CUtensorMap& tm_v,
+                                            const int32_t* block_of_slot, const int32_t* ctx_len,
+                                            float scale, uint16_t* out, cudaStream_t st,
+                                            const DeviceInfo& di);
+
 // Attention of one layer and scoring of another in one launch (same shapes).
 cudaError_t fused_configure();  // one-time function attributes
 cudaError_t launch_attend_and_score(const Shape& s, const CUtensorMap& tm_k,

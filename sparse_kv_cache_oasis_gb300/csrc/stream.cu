@@ -43,8 +43,10 @@ __global__ void __launch_bounds__(kFusedThreads) attn_score_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
   if (c < nA && warp < kAttnWarps) {
-    attn_cta(&tm_k, &tm_v, q, block_of_slot, ctx_len, scale_log2, out, Hq, Hkv, G, S, NB, P, err,
-             smem, c / P, c % P, warp, lane, [] { attn_warps_barrier(); });
+    const int u = c / P, b = u / Hkv, h = u - b * Hkv;
+    const GroupRows rows{q, out, (static_cast<int64_t>(b) * Hq + h * G) * kHeadDim};
+    attn_cta<1>(&tm_k, &tm_v, rows, G, block_of_slot, ctx_len, scale_log2, Hkv, S, NB, P, err, smem,
+                u, c % P, warp, lane, [] { attn_warps_barrier(); });
     return;
   }
   // scoring warps (all ten in a scoring-only CTA): this CTA's tiles, then a

@@ -87,6 +87,7 @@ class LayerState:
         self.n_fetch = torch.zeros((B, H), dtype=i32, device=dev)
         self.n_evict = torch.zeros((B, H), dtype=i32, device=dev)
         self.out = torch.empty((B, Hq, D), dtype=bf, device=dev)
+        self.out_joint = torch.empty((B, L + 1, Hq, D), dtype=bf, device=dev)  # decoded + drafts
         self.clock = torch.zeros((B, H), dtype=i32, device=dev)  # device step per (b, h)
         self.workspace = torch.zeros(max(ob.oasis_attn_workspace_bytes(c), 256), dtype=torch.uint8,
                                      device=dev)
@@ -98,6 +99,13 @@ class LayerState:
     def attention(self, q, stream=None):
         ob.oasis_sparse_decode_attn(self.cfg, q, self.pool_k, self.pool_v, self.block_of_slot,
                                     self.ctx_len, self.scale, self.out, self.workspace, stream)
+
+    def attention_joint(self, q, q_draft, stream=None):
+        """Attention of the decoded token and the draft tokens in one pass:
+        self.out_joint[:, 0] for q, self.out_joint[:, l] for q_draft[:, l-1]."""
+        ob.oasis_sparse_decode_attn_joint(self.cfg, q, q_draft, self.pool_k, self.pool_v,
+                                          self.block_of_slot, self.ctx_len, self.scale,
+                                          self.out_joint, stream)
 
     def attention_and_score(self, q, other, q_draft, stream=None):
         """This layer's attention and `other` layer's scoring in one launch."""

@@ -1,6 +1,7 @@
 """C-ABI checks that need no GPU: the library loads, exports every symbol the
 header declares, and rejects bad arguments before launching anything."""
 import ctypes as C
+import math
 import os
 import subprocess
 
@@ -104,6 +105,10 @@ def test_entry_points_reject_bad_arguments_before_launch(lib):
     assert L.oasis_sparse_decode_attn(C.byref(c), ok, ok, ok, ok, null, -1.0, ok, ok, ws, null) == ob.OASIS_ERR_INVALID_ARG
     assert L.oasis_sparse_decode_attn(C.byref(c), ok, ok, ok, ok, null, 0.1, ok, P(0x10010), ws, null) == ob.OASIS_ERR_INVALID_ARG
     assert L.oasis_sparse_decode_attn(C.byref(c), ok, ok, ok, ok, null, 0.1, ok, ok, ws - 1, null) == ob.OASIS_ERR_INVALID_ARG
+    # joint attention: the draft queries and the output are checked like q
+    assert L.oasis_sparse_decode_attn_joint(C.byref(c), ok, odd, ok, ok, ok, null, 0.1, ok, null) == ob.OASIS_ERR_INVALID_ARG
+    assert L.oasis_sparse_decode_attn_joint(C.byref(c), ok, ok, ok, ok, ok, null, 0.1, null, null) == ob.OASIS_ERR_INVALID_ARG
+    assert L.oasis_sparse_decode_attn_joint(C.byref(c), ok, ok, ok, ok, ok, null, math.inf, ok, null) == ob.OASIS_ERR_INVALID_ARG
     bad = ob.OasisConfig.make(dict(W.TINY.config(), head_dim=64))
     assert L.oasis_score_blocks(C.byref(bad), ok, ok, ok, null) == ob.OASIS_ERR_UNSUPPORTED
     assert L.oasis_select_topk(None, ok, ok, null) == ob.OASIS_ERR_INVALID_ARG

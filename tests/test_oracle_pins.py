@@ -443,6 +443,48 @@ def test_attention_closed_forms_and_masking():
     assert not out.any()
 
 
+def test_joint_attention_rows_follow_their_tokens():
+    """Joint attention: output row l of request b, head n attends with draft
+    token l-1's query (row 0: the decoded token's).  Keys are one-hot per
+    token and every query points hard at one token, so each output row is
+    that token's value row; a masked target falls back to the mean of the
+    visible values."""
+    B, G, Hkv, L, S = 2, 2, 2, 3, 4
+    Hq = G * Hkv
+    cfg = small_cfg(batch=B, num_q_heads=Hq, num_kv_heads=Hkv, num_blocks=6,
+                    kv_budget_tokens=16 * S, lookahead=L, top_k=4)
+    rs = np.random.default_rng(31)
+    pk = np.zeros((B, Hkv, S, 16, 128), np.float32)
+    for s_ in range(S):
+        for t in range(16):
+            pk[:, :, s_, t, 16 * s_ + t] = 1.0                      # token (slot s_, t) -> e_{16 s_ + t}
+    pvb = bf(rs.standard_normal((B, Hkv, S, 16, 128)).astype(np.float32))
+    pkb = bf(pk)
+    bos = np.asarray([[[3, 0, 5, 1], [2, 4, 1, 0]], [[0, 1, 2, 3], [5, 4, 3, 2]]], np.int32)
+    target = rs.integers(0, 16 * S, size=(B, L + 1, Hq))             # token index 16*slot + t
+    qrows = np.zeros((B, L + 1, Hq, 128), np.float32)
+    for b, l, n in itertools.product(range(B), range(L + 1), range(Hq)):
+        qrows[b, l, n, target[b, l, n]] = 40.0
+    q, qd = bf(qrows[:, 0]), bf(qrows[:, 1:])
+    out = oracle.sparse_decode_attn_joint(cfg, q, qd, pkb, pvb, bos, None, 1.0)
+    assert out.shape == (B, L + 1, Hq, 128)
+    vf = f32(pvb).reshape(B, Hkv, 16 * S, 128)
+    for b, l, n in itertools.product(range(B), range(L + 1), range(Hq)):
+        assert np.allclose(out[b, l, n], vf[b, n // G, target[b, l, n]], atol=1e-12)
+    # row 0 is the plain attention of q
+    assert np.array_equal(out[:, 0], oracle.sparse_decode_attn(cfg, q, pkb, pvb, bos, None, 1.0))
+    # one context length for all rows: request 0 sees blocks 0 and 1 only
+    # (positions < 32), i.e. slots holding blocks 0, 1 of each KV head
+    ctx = np.asarray([32, 96], np.int32)
+    out = oracle.sparse_decode_attn_joint(cfg, q, qd, pkb, pvb, bos, ctx, 1.0)
+    for h in range(Hkv):
+        vis = [16 * s_ + t for s_ in range(S) if bos[0, h, s_] < 2 for t in range(16)]
+        for l, g in itertools.product(range(L + 1), range(G)):
+            n = h * G + g
+            want = vf[0, h, target[0, l, n]] if target[0, l, n] in vis else vf[0, h, vis].mean(0)
+            assert np.allclose(out[0, l, n], want, atol=1e-12)
+
+
 # ----------------------------------------------------------------------------
 # planted recovery on the tiny workload (seeded expectation)
 # ----------------------------------------------------------------------------
