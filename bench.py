@@ -62,6 +62,8 @@ def parse():
                     help="only run this many untimed graph steps (for ncu launch lists)")
     ap.add_argument("--profile-joint", type=int, default=0,
                     help="with --profile-steps: then this many joint-attention launches")
+    ap.add_argument("--profile-minmax", type=int, default=0,
+                    help="with --profile-steps: then this many min/max-key scoring launches")
     return ap.parse_args()
 
 
@@ -116,7 +118,8 @@ def algorithmic_bytes(wl, n_fetch_blocks: float, valid_slots: float):
     rows_io = wl.batch * wl.num_q_heads * wl.head_dim * 2 * (1 + wl.lookahead)
     joint = valid_slots * blk + 2 * rows_io + U * wl.slots * 4
     return dict(attn=attn, score=score, fused=attn + score, topk=topk, plan=plan, fetch=fetch_hbm,
-                hbm=attn + score + topk + plan + fetch_hbm, link=link, joint=joint)
+                hbm=attn + score + topk + plan + fetch_hbm, link=link, joint=joint,
+                score_mm=score)  # bf16 max + min rows: as many bytes as the fp32 mean
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -544,9 +547,14 @@ def gpu_arm(args):
         run_steps(0, args.profile_steps)
         for r in range(args.profile_joint):  # joint attention launches after the steps
             layers[r % n_inst].attention_joint(q_dev[r % n_inst][0], qd_dev[r % n_inst][0], compute)
+        if args.profile_minmax:
+            for L in layers:
+                L.build_minmax_summaries()
+        for r in range(args.profile_minmax):  # then min/max scoring launches
+            layers[r % n_inst].score_minmax(qd_dev[r % n_inst][0], compute)
         torch.cuda.synchronize()
-        print(json.dumps({"profile_steps": args.profile_steps, "profile_joint": args.profile_joint}),
-              flush=True)
+        print(json.dumps({"profile_steps": args.profile_steps, "profile_joint": args.profile_joint,
+                          "profile_minmax": args.profile_minmax}), flush=True)
         return
 
     # ---- warm-up and timed region
@@ -600,9 +608,14 @@ def gpu_arm(args):
                                           qd_dev[(i + 1) % n_inst][0], compute)
                 elif kind == "joint":
                     L.attention_joint(q_dev[i][0], qd_dev[i][0], compute)
+                elif kind == "score_mm":
+                    L.score_minmax(qd_dev[i][0], compute)
         return g
 
-    kinds = ["attn", "score", "topk", "fused", "joint"]
+    for L in layers:  # min/max compressed keys for the scoring variant (set-up)
+        L.build_minmax_summaries()
+    torch.cuda.synchronize()
+    kinds = ["attn", "score", "topk", "fused", "joint", "score_mm"]
     mean_ms = {}
     for kind in kinds:
         g = kernel_graph(kind)
@@ -718,6 +731,12 @@ def gpu_arm(args):
                 "achieved_gbs": by["joint"] / (mean_ms["joint"] * 1e-3) / 1e9,
                 "frac_of_measured_hbm": by["joint"] / (mean_ms["joint"] * 1e-3) / 1e9 / peak,
                 "vs_single_query_attention": mean_ms["joint"] / mean_ms["attn"]},
+            "minmax_scoring": {
+                "kernel": "score_kernel (min/max keys)", "ms_per_launch": mean_ms["score_mm"],
+                "bytes_per_launch": by["score_mm"],
+                "achieved_gbs": by["score_mm"] / (mean_ms["score_mm"] * 1e-3) / 1e9,
+                "frac_of_measured_hbm": by["score_mm"] / (mean_ms["score_mm"] * 1e-3) / 1e9 / peak,
+                "vs_mean_scoring": mean_ms["score_mm"] / mean_ms["score"]},
             "kernels_ms": mean_ms,
             "kernel_gbs": {k: by[k] / (mean_ms[k] * 1e-3) / 1e9 for k in kinds},
             "gpu_launches": args.steps * 4,

@@ -13,6 +13,7 @@
  *   oasis_attend_and_score     attention of one layer + scoring of another in one launch (Fig. 8)
  *   oasis_sparse_decode_attn_joint  decoded + draft tokens in one pass of the working set (Fig. 7 right)
  *   oasis_score_blocks         draft queries scan compressed keys  (Fig. 7 right)
+ *   oasis_score_blocks_minmax  the same against min/max-pooled keys (Fig. 7 left)
  *   oasis_select_topk          top-K blocks per KV head            (diagram step 2)
  *   oasis_plan_fetch           diff vs. working set, capped LRU    (diagram step 3, Tab. 2)
  *   oasis_fetch_blocks         host -> HBM transfer, copy stream   (diagram step 4, Fig. 8)
@@ -43,6 +44,7 @@
  * KV head h):
  *   host K, V       [B][Hkv][NB][bs][D]  bf16  full cache, pinned host
  *   summ            [B][Hkv][NB][D]      fp32  compressed keys (block means)
+ *   summ_mm         [B][Hkv][NB][2][D]   bf16  min/max compressed keys (max row, min row)
  *   q_draft         [B][L][Hq][D]        bf16  draft-token queries
  *   scores          [B][Hkv][NB]         fp32
  *   topk_ids        [B][Hkv][K]          int32 in priority order
@@ -125,6 +127,29 @@ oasis_status_t oasis_build_summaries(const oasis_config_t* cfg, const uint16_t* 
  * value.  q_draft and summ 16-byte aligned. */
 oasis_status_t oasis_score_blocks(const oasis_config_t* cfg, const uint16_t* q_draft,
                                   const float* summ, float* scores, void* stream);
+
+/* Min/max compressed keys, the pooling [OasisKV] Fig. 7 (left) names:
+ *   summ_mm[b,h,j,0,:] = elementwise max of the bs keys of block j,
+ *   summ_mm[b,h,j,1,:] = elementwise min,
+ * bf16 values copied from the keys (exact; on equal values the earlier
+ * token's bit pattern, which decides +0 / -0).  Layout [B][Hkv][NB][2][D]
+ * bf16: 512 bytes per block, as many as the fp32 mean.  Set-up work, like
+ * oasis_build_summaries; k and summ_mm 16-byte aligned. */
+oasis_status_t oasis_build_summaries_minmax(const oasis_config_t* cfg, const uint16_t* k,
+                                            uint16_t* summ_mm, void* stream);
+
+/* Look-ahead scoring against min/max compressed keys:
+ *   scores[b,h,j] = max over l < L, g < G of
+ *                   sum_d max(q_d * min_d, q_d * max_d),  q = q_draft[b,l,h*G+g,:],
+ * an upper bound of q . k for every key k of the block.  Computed as the dot
+ * product of [max(q,0) | min(q,0)] with [max | min] on bf16 tensor cores:
+ * exact products, fp32 accumulation of 256 terms (error at most about
+ * 256 * 2^-23 of sum_d |q_d| * max(|min_d|, |max_d|)).  Same scores layout as
+ * oasis_score_blocks, so oasis_select_topk and the planning follow unchanged.
+ * L*G <= 32 (else OASIS_ERR_UNSUPPORTED).  q_draft and summ_mm 16-byte
+ * aligned, scores 8-byte aligned. */
+oasis_status_t oasis_score_blocks_minmax(const oasis_config_t* cfg, const uint16_t* q_draft,
+                                         const uint16_t* summ_mm, float* scores, void* stream);
 
 /* Per-KV-head top-K ([OasisKV] diagram step 2, Fig. 4).  Forced blocks (sink
  * and local window) come first in ascending id and count toward K; the other

@@ -60,6 +60,8 @@ def lib():
                 "orc_fetch_cap": (C.c_int, [cfgp]),
                 "orc_build_summaries": (None, [cfgp, P, P]),
                 "orc_score_blocks": (None, [cfgp, P, P, P]),
+                "orc_build_summaries_minmax": (None, [cfgp, P, P]),
+                "orc_score_blocks_minmax": (None, [cfgp, P, P, P]),
                 "orc_select_topk": (C.c_int, [cfgp, P, P]),
                 "orc_plan_fetch": (C.c_int, [cfgp, P, C.c_int32, P, P, P, P, P, P, P, P]),
                 "orc_fetch_blocks": (C.c_int, [cfgp, P, P, P, P, P, P, P]),
@@ -144,6 +146,26 @@ def score_blocks(cfg: dict, q_draft: np.ndarray, summ: np.ndarray) -> np.ndarray
     out = np.empty((B, H, NB), dtype=np.float32)
     lib().orc_score_blocks(C.byref(_cfg(cfg)), _p(q_draft, np.uint16), _p(summ, np.float32),
                            _p(out, np.float32))
+    return out
+
+
+def build_summaries_minmax(cfg: dict, k: np.ndarray) -> np.ndarray:
+    """[B, H, NB, 2, D] bf16 bits: per block the elementwise max (row 0) and
+    min (row 1) of its keys."""
+    B, H, Hq, NB, bs, D, S = _sizes(cfg)
+    _check(k, (B, H, NB, bs, D), "k")
+    out = np.empty((B, H, NB, 2, D), dtype=np.uint16)
+    lib().orc_build_summaries_minmax(C.byref(_cfg(cfg)), _p(k, np.uint16), _p(out, np.uint16))
+    return out
+
+
+def score_blocks_minmax(cfg: dict, q_draft: np.ndarray, summ_mm: np.ndarray) -> np.ndarray:
+    B, H, Hq, NB, bs, D, S = _sizes(cfg)
+    _check(q_draft, (B, cfg["lookahead"], Hq, D), "q_draft")
+    _check(summ_mm, (B, H, NB, 2, D), "summ_mm")
+    out = np.empty((B, H, NB), dtype=np.float32)
+    lib().orc_score_blocks_minmax(C.byref(_cfg(cfg)), _p(q_draft, np.uint16),
+                                  _p(summ_mm, np.uint16), _p(out, np.float32))
     return out
 
 

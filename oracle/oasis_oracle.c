@@ -117,6 +117,67 @@ void orc_score_blocks(const orc_cfg* c, const uint16_t* q_draft, const float* su
             }
 }
 
+/*
+ * Min/max compressed keys, [OasisKV] Fig. 7 (left): the page pools each block
+ * by its minimum and maximum.  Per dimension d of block j, the largest and
+ * the smallest of the block's bs key values, kept as the bf16 key value
+ * itself; row 0 of the block's pair is the max, row 1 the min.  Reading: where
+ * several tokens hold the extreme value, the first in token order gives the
+ * stored bit pattern (this only decides between +0 and -0).
+ */
+void orc_build_summaries_minmax(const orc_cfg* c, const uint16_t* k, uint16_t* summ_mm)
+{
+    const int B = c->batch, H = c->num_kv_heads, NB = c->num_blocks;
+    const int bs = c->block_size, D = c->head_dim;
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h)
+            for (int j = 0; j < NB; ++j)
+                for (int d = 0; d < D; ++d) {
+                    const size_t blk = ((size_t)b * H + h) * NB + j;
+                    uint16_t hi = k[(blk * bs) * D + d], lo = hi;
+                    for (int t = 1; t < bs; ++t) {
+                        uint16_t x = k[(blk * bs + t) * D + d];
+                        if (bf16_to_double(x) > bf16_to_double(hi)) hi = x;
+                        if (bf16_to_double(x) < bf16_to_double(lo)) lo = x;
+                    }
+                    summ_mm[(blk * 2 + 0) * D + d] = hi;
+                    summ_mm[(blk * 2 + 1) * D + d] = lo;
+                }
+}
+
+/*
+ * Look-ahead scoring against min/max compressed keys ([OasisKV] Fig. 7): for
+ * each draft query q (every l < L, g < G of KV head h) the block's bound
+ *   sum_d max(q_d * min_d, q_d * max_d),
+ * the largest q . k any key k inside the block's per-dimension box can give;
+ * the block's score is the maximum over (l, g), as for the mean keys.
+ */
+void orc_score_blocks_minmax(const orc_cfg* c, const uint16_t* q_draft, const uint16_t* summ_mm,
+                             float* scores)
+{
+    const int B = c->batch, H = c->num_kv_heads, Hq = c->num_q_heads;
+    const int G = Hq / H, L = c->lookahead, NB = c->num_blocks, D = c->head_dim;
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h)
+            for (int j = 0; j < NB; ++j) {
+                const uint16_t* mx = summ_mm + ((((size_t)b * H + h) * NB + j) * 2 + 0) * D;
+                const uint16_t* mn = summ_mm + ((((size_t)b * H + h) * NB + j) * 2 + 1) * D;
+                double best = -INFINITY;
+                for (int l = 0; l < L; ++l)
+                    for (int g = 0; g < G; ++g) {
+                        const uint16_t* q = q_draft + (((size_t)b * L + l) * Hq + (size_t)h * G + g) * D;
+                        double bound = 0.0;
+                        for (int d = 0; d < D; ++d) {
+                            double qd = bf16_to_double(q[d]);
+                            double lo = qd * bf16_to_double(mn[d]), hi = qd * bf16_to_double(mx[d]);
+                            bound += lo > hi ? lo : hi;
+                        }
+                        if (bound > best) best = bound;
+                    }
+                scores[((size_t)b * H + h) * NB + j] = (float)best;
+            }
+}
+
 /* Forced blocks: the sink [0, sink) and the local window, the last `local`
  * blocks of the context.  They are always selected and count toward K. */
 static int is_forced(const orc_cfg* c, int j)

@@ -59,6 +59,9 @@ int orc_fetch_cap(const orc_cfg* c);
 void orc_build_summaries(const orc_cfg* c, const uint16_t* k, float* summ);
 void orc_score_blocks(const orc_cfg* c, const uint16_t* q_draft, const float* summ,
                       float* scores);
+void orc_build_summaries_minmax(const orc_cfg* c, const uint16_t* k, uint16_t* summ_mm);
+void orc_score_blocks_minmax(const orc_cfg* c, const uint16_t* q_draft, const uint16_t* summ_mm,
+                             float* scores);
 int  orc_select_topk(const orc_cfg* c, const float* scores, int32_t* topk_ids);
 int  orc_plan_fetch(const orc_cfg* c, const int32_t* topk_ids, int32_t step,
                     int32_t* slot_of_block, int32_t* block_of_slot, int32_t* last_used,

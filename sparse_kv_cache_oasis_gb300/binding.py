@@ -68,6 +68,8 @@ _SIGS = {
                                          _P, _P, _P, _P, _P]),
     "oasis_sparse_decode_attn_joint": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P, _P, _P, _P,
                                                  C.c_float, _P, _P]),
+    "oasis_build_summaries_minmax": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P]),
+    "oasis_score_blocks_minmax": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P, _P]),
     "oasis_host_register": (C.c_int, [_P, C.c_size_t, C.POINTER(C.c_void_p)]),
     "oasis_host_unregister": (C.c_int, [_P]),
     "oasis_device_errors": (C.c_int, [C.POINTER(C.c_uint32), C.c_int32]),
@@ -176,6 +178,25 @@ def oasis_score_blocks(cfg, q_draft, summ, scores, stream=None) -> None:
     _check("oasis_score_blocks", lib().oasis_score_blocks(
         C.byref(c), _ptr(q_draft, torch.bfloat16, (B, c.lookahead, Hq, D), "q_draft"),
         _ptr(summ, torch.float32, (B, H, NB, D), "summ"),
+        _ptr(scores, torch.float32, (B, H, NB), "scores"), _stream(stream)))
+
+
+def oasis_build_summaries_minmax(cfg, k, summ_mm, stream=None) -> None:
+    """Per-block elementwise max and min keys, [B, Hkv, NB, 2, D] bf16."""
+    c = OasisConfig.make(cfg)
+    B, H, Hq, NB, bs, D, S = _dims(c)
+    kp = _ptr(k, torch.bfloat16, (B, H, NB, bs, D), "k", device=False)
+    sp = _ptr(summ_mm, torch.bfloat16, (B, H, NB, 2, D), "summ_mm")
+    _check("oasis_build_summaries_minmax",
+           lib().oasis_build_summaries_minmax(C.byref(c), kp, sp, _stream(stream)))
+
+
+def oasis_score_blocks_minmax(cfg, q_draft, summ_mm, scores, stream=None) -> None:
+    c = OasisConfig.make(cfg)
+    B, H, Hq, NB, bs, D, S = _dims(c)
+    _check("oasis_score_blocks_minmax", lib().oasis_score_blocks_minmax(
+        C.byref(c), _ptr(q_draft, torch.bfloat16, (B, c.lookahead, Hq, D), "q_draft"),
+        _ptr(summ_mm, torch.bfloat16, (B, H, NB, 2, D), "summ_mm"),
         _ptr(scores, torch.float32, (B, H, NB), "scores"), _stream(stream)))
 
 

@@ -216,6 +216,32 @@ oasis_status_t oasis_score_blocks(const oasis_config_t* cfg, const uint16_t* q_d
   return from_cuda(launch_score_blocks(s, q_draft, summ, scores, static_cast<cudaStream_t>(stream), di));
 }
 
+oasis_status_t oasis_build_summaries_minmax(const oasis_config_t* cfg, const uint16_t* k,
+                                            uint16_t* summ_mm, void* stream) {
+  Shape s;
+  oasis_status_t st = make_shape(cfg, &s);
+  if (st != OASIS_OK) return st;
+  if (!aligned(k, 16) || !aligned(summ_mm, 16)) return OASIS_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != OASIS_OK) return st;
+  return from_cuda(
+      launch_build_summaries_minmax(s, k, summ_mm, static_cast<cudaStream_t>(stream), di));
+}
+
+oasis_status_t oasis_score_blocks_minmax(const oasis_config_t* cfg, const uint16_t* q_draft,
+                                         const uint16_t* summ_mm, float* scores, void* stream) {
+  Shape s;
+  oasis_status_t st = make_shape(cfg, &s);
+  if (st != OASIS_OK) return st;
+  if (s.L * s.G > 32) return OASIS_ERR_UNSUPPORTED;
+  if (!aligned(q_draft, 16) || !aligned(summ_mm, 16) || !aligned(scores, 8))
+    return OASIS_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != OASIS_OK) return st;
+  return from_cuda(
+      launch_score_blocks_minmax(s, q_draft, summ_mm, scores, static_cast<cudaStream_t>(stream), di));
+}
+
 oasis_status_t oasis_select_topk(const oasis_config_t* cfg, const float* scores,
                                  int32_t* topk_ids, void* stream) {
   Shape s;

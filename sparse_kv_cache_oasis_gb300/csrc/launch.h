@@ -30,6 +30,11 @@ cudaError_t launch_build_summaries(const Shape& s, const uint16_t* k, float* sum
                                    cudaStream_t st, const DeviceInfo& di);
 cudaError_t launch_score_blocks(const Shape& s, const uint16_t* q_draft, const float* summ,
                                 float* scores, cudaStream_t st, const DeviceInfo& di);
+cudaError_t launch_build_summaries_minmax(const Shape& s, const uint16_t* k, uint16_t* summ_mm,
+                                          cudaStream_t st, const DeviceInfo& di);
+cudaError_t launch_score_blocks_minmax(const Shape& s, const uint16_t* q_draft,
+                                       const uint16_t* summ_mm, float* scores, cudaStream_t st,
+                                       const DeviceInfo& di);
 cudaError_t launch_select_topk(const Shape& s, const float* scores, int32_t* topk_ids,
                                cudaStream_t st, const DeviceInfo& di);
 cudaError_t launch_plan_fetch(const Shape& s, const int32_t* topk_ids, int32_t step,

@@ -44,9 +44,9 @@ constexpr int kScoreThreads = 192;
 constexpr int kScoreWarps = kScoreThreads / 32;
 constexpr int kMinTilesPerCta = 16;
 
-template <int MT>
+template <int MT, int KIND>
 __global__ void __launch_bounds__(kScoreThreads) score_kernel(
-    const uint16_t* __restrict__ q_draft, const float* __restrict__ summ,
+    const uint16_t* __restrict__ q_draft, const float4* __restrict__ summ,
     float* __restrict__ scores, int L, int Hq, int Hkv, int G, int NB, int T, int Rt) {
   // shared memory: one ring per warp of kScoreStages tiles, each [p][lane]
   // float4 (a lane reads back what it copied)
@@ -58,16 +58,16 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(
   const int qw = (t_hi - t_lo + kScoreWarps - 1) / kScoreWarps;
   const int w_lo = t_lo + warp * qw < t_hi ? t_lo + warp * qw : t_hi;
   const int tpw = w_lo + qw < t_hi ? qw : t_hi - w_lo;
-  score_warp_range<MT>(q_draft, summ, scores, L, Hq, Hkv, G, NB, w_lo, tpw,
-                       smem4 + warp * kScoreStages * 8 * 32, lane);
+  score_warp_range<MT, KIND>(q_draft, summ, scores, L, Hq, Hkv, G, NB, w_lo, tpw,
+                             smem4 + warp * kScoreStages * 8 * 32, lane);
 }
 
 static size_t score_smem_bytes(int) {
   return sizeof(float4) * static_cast<size_t>(kScoreWarps) * kScoreStages * 8 * 32;
 }
 
-template <int MT>
-static cudaError_t launch_mt(const Shape& s, const uint16_t* q_draft, const float* summ,
+template <int MT, int KIND>
+static cudaError_t launch_mt(const Shape& s, const uint16_t* q_draft, const void* summ,
                              float* scores, cudaStream_t st, const DeviceInfo& di) {
   // one CTA per SM over equal contiguous tile ranges
   const int ntiles = (s.NB + 7) / 8;
@@ -78,8 +78,9 @@ static cudaError_t launch_mt(const Shape& s, const uint16_t* q_draft, const floa
   if (C < 1) C = 1;
   const int64_t Rt = (T + C - 1) / C;
   const int64_t grid = (T + Rt - 1) / Rt;
-  score_kernel<MT><<<static_cast<unsigned>(grid), kScoreThreads, score_smem_bytes(MT), st>>>(
-      q_draft, summ, scores, s.L, s.Hq, s.Hkv, s.G, s.NB, static_cast<int>(T), static_cast<int>(Rt));
+  score_kernel<MT, KIND><<<static_cast<unsigned>(grid), kScoreThreads, score_smem_bytes(MT), st>>>(
+      q_draft, static_cast<const float4*>(summ), scores, s.L, s.Hq, s.Hkv, s.G, s.NB,
+      static_cast<int>(T), static_cast<int>(Rt));
   return cudaGetLastError();
 }
 
@@ -87,35 +88,49 @@ cudaError_t launch_score_blocks(const Shape& s, const uint16_t* q_draft, const f
                                 float* scores, cudaStream_t st, const DeviceInfo& di) {
   const int mt = (s.L * s.G + 15) / 16;
   switch (mt) {
-    case 1: return launch_mt<1>(s, q_draft, summ, scores, st, di);
-    case 2: return launch_mt<2>(s, q_draft, summ, scores, st, di);
-    case 3: return launch_mt<3>(s, q_draft, summ, scores, st, di);
-    case 4: return launch_mt<4>(s, q_draft, summ, scores, st, di);
+    case 1: return launch_mt<1, kSummMean>(s, q_draft, summ, scores, st, di);
+    case 2: return launch_mt<2, kSummMean>(s, q_draft, summ, scores, st, di);
+    case 3: return launch_mt<3, kSummMean>(s, q_draft, summ, scores, st, di);
+    case 4: return launch_mt<4, kSummMean>(s, q_draft, summ, scores, st, di);
     default: return cudaErrorInvalidValue;  // rejected earlier by validation (L*G <= 64)
   }
 }
 
-template <int MT>
+cudaError_t launch_score_blocks_minmax(const Shape& s, const uint16_t* q_draft,
+                                       const uint16_t* summ_mm, float* scores, cudaStream_t st,
+                                       const DeviceInfo& di) {
+  const int mt = (s.L * s.G + 15) / 16;
+  switch (mt) {
+    case 1: return launch_mt<1, kSummMinMax>(s, q_draft, summ_mm, scores, st, di);
+    case 2: return launch_mt<2, kSummMinMax>(s, q_draft, summ_mm, scores, st, di);
+    default: return cudaErrorInvalidValue;  // rejected earlier by validation (L*G <= 32)
+  }
+}
+
+template <int MT, int KIND>
 static cudaError_t score_configure_mt() {
-  cudaError_t e = cudaFuncSetAttribute(score_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const auto fn = score_kernel<MT, KIND>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(score_smem_bytes(MT)));
   if (e == cudaSuccess)  // largest carve-out: the step's other kernels share the SM
-    e = cudaFuncSetAttribute(score_kernel<MT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
   return e;
 }
 
 cudaError_t score_configure() {
-  cudaError_t e = score_configure_mt<1>();
-  if (e == cudaSuccess) e = score_configure_mt<2>();
-  if (e == cudaSuccess) e = score_configure_mt<3>();
-  if (e == cudaSuccess) e = score_configure_mt<4>();
+  cudaError_t e = score_configure_mt<1, kSummMean>();
+  if (e == cudaSuccess) e = score_configure_mt<2, kSummMean>();
+  if (e == cudaSuccess) e = score_configure_mt<3, kSummMean>();
+  if (e == cudaSuccess) e = score_configure_mt<4, kSummMean>();
+  if (e == cudaSuccess) e = score_configure_mt<1, kSummMinMax>();
+  if (e == cudaSuccess) e = score_configure_mt<2, kSummMinMax>();
   return e;
 }
 
 int score_ctas_per_sm() {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, score_kernel<1>, kScoreThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, score_kernel<1, kSummMean>, kScoreThreads,
                                                     score_smem_bytes(1)) != cudaSuccess)
     return 2;
   return n > 0 ? n : 1;

@@ -31,9 +31,90 @@ constexpr uint32_t kTf32Mask = 0xFFFFE000u;  // sign, exponent, 10 mantissa bits
 // each use (to bound the registers).
 __host__ __device__ constexpr int frag_words(int mt) { return mt == 1 ? 8 : 4; }
 
+// Compressed-key kinds: the fp32 mean key of a block, or its elementwise max
+// and min keys (bf16, [max(D) | min(D)] per block).  Both are 512 bytes per
+// block, so the streaming below is the same; only the contraction differs.
+constexpr int kSummMean = 0;
+constexpr int kSummMinMax = 1;
+constexpr int kMaxMinMaxTiles = 2;  // min/max scoring keeps every A fragment unpacked
+
+// Words per (16-row tile, chunk p) of a lane's A fragments.
+__host__ __device__ constexpr int q_words(int mt, int kind) {
+  return kind == kSummMinMax ? 8 : frag_words(mt);
+}
+
+// Max over the valid query rows of a tile's accumulators (rows >= M are
+// padding), then the 8 block scores are written out.
+template <int MT>
+__device__ __forceinline__ void score_store(const float (&acc)[MT][4], int g, int t, int M, int n0,
+                                            int NB, int64_t out_off, float* out) {
+  float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    if (16 * mt + g < M) {
+      m0 = fmaxf(m0, acc[mt][0]);
+      m1 = fmaxf(m1, acc[mt][1]);
+    }
+    if (16 * mt + g + 8 < M) {
+      m0 = fmaxf(m0, acc[mt][2]);
+      m1 = fmaxf(m1, acc[mt][3]);
+    }
+  }
+  m0 = warp_max_xor_g(m0);
+  m1 = warp_max_xor_g(m1);
+  if (g == 0) {
+    const int col = n0 + 2 * t;
+    // a float2 store needs an even element offset (out_off + col); odd NB breaks it
+    const bool even = ((out_off + col) & 1) == 0;
+    if (col + 1 < NB && even) {
+      __stcs(reinterpret_cast<float2*>(out + col), make_float2(m0, m1));
+    } else {
+      if (col < NB) out[col] = m0;
+      if (col + 1 < NB) out[col + 1] = m1;
+    }
+  }
+}
+
+// Min/max scores of 8 blocks (one tile).  Per dimension
+//   max(q*mn, q*mx) = max(q, 0)*mx + min(q, 0)*mn     (mx >= mn),
+// so a block's score is one 256-long dot product of [q+ | q-] with
+// [mx | mn]: every operand is a bf16 value (a sign mask splits q), the
+// products are exact in fp32, and bf16 MMAs (m16n8k16, fp32 accumulation)
+// take it.  Lane (g, t)'s 16 bytes of chunk p hold k-steps 2p and 2p+1.
+template <int MT>
+__device__ __forceinline__ void score_tile_minmax(const float4 (&v)[8],
+                                                  const uint32_t (&wq)[MT][8][8], int g, int t,
+                                                  int M, int n0, int NB, int64_t out_off,
+                                                  float* out) {
+  float acc[MT][4], acc1[MT][4], acc2[MT][4], acc3[MT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[mt][r] = acc1[mt][r] = acc2[mt][r] = acc3[mt][r] = 0.f;
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    const uint32_t x = __float_as_uint(v[p].x), y = __float_as_uint(v[p].y);
+    const uint32_t z = __float_as_uint(v[p].z), w = __float_as_uint(v[p].w);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      // rows g and g+8: words 0-3 of the chunk are wq[..][0-3] and [4-7]
+      const uint32_t a[4] = {wq[mt][p][0], wq[mt][p][4], wq[mt][p][1], wq[mt][p][5]};
+      const uint32_t c[4] = {wq[mt][p][2], wq[mt][p][6], wq[mt][p][3], wq[mt][p][7]};
+      mma_bf16_16816((p & 1) ? acc2[mt] : acc[mt], a, x, y);   // k-step 2p
+      mma_bf16_16816((p & 1) ? acc3[mt] : acc1[mt], c, z, w);  // k-step 2p+1
+    }
+  }
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[mt][r] = (acc[mt][r] + acc2[mt][r]) + (acc1[mt][r] + acc3[mt][r]);
+  score_store<MT>(acc, g, t, M, n0, NB, out_off, out);
+}
+
 // Scores of 8 blocks (one tile) from their summaries in v; writes them out.
 template <int MT>
-__device__ __forceinline__ void score_tile(const float4 (&v)[8], const uint32_t (&wq)[MT][8][frag_words(MT)], int lane, int g,
+__device__ __forceinline__ void score_tile(const float4 (&v)[8],
+                                           const uint32_t (&wq)[MT][8][frag_words(MT)], int g,
                                            int t, int M, int n0, int NB, int64_t out_off,
                                            float* out) {
   // four independent accumulator chains (hi/lo x even/odd k-step) keep the
@@ -73,43 +154,20 @@ __device__ __forceinline__ void score_tile(const float4 (&v)[8], const uint32_t 
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
     for (int r = 0; r < 4; ++r) acc[mt][r] = (acc[mt][r] + acc2[mt][r]) + (acc1[mt][r] + acc3[mt][r]);
-  // max over the valid query rows (rows >= L*G are padding)
-  float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    if (16 * mt + g < M) {
-      m0 = fmaxf(m0, acc[mt][0]);
-      m1 = fmaxf(m1, acc[mt][1]);
-    }
-    if (16 * mt + g + 8 < M) {
-      m0 = fmaxf(m0, acc[mt][2]);
-      m1 = fmaxf(m1, acc[mt][3]);
-    }
-  }
-  m0 = warp_max_xor_g(m0);
-  m1 = warp_max_xor_g(m1);
-  if (g == 0) {
-    const int col = n0 + 2 * t;
-    // a float2 store needs an even element offset (out_off + col); odd NB breaks it
-    const bool even = ((out_off + col) & 1) == 0;
-    if (col + 1 < NB && even) {
-      __stcs(reinterpret_cast<float2*>(out + col), make_float2(m0, m1));
-    } else {
-      if (col < NB) out[col] = m0;
-      if (col + 1 < NB) out[col + 1] = m1;
-    }
-  }
+  score_store<MT>(acc, g, t, M, n0, NB, out_off, out);
 }
 
 // One warp's share of the scoring: the contiguous tiles [w_lo, w_lo + tpw) of
 // the global tile list (8 blocks per tile), streamed through `ring`
-// (kScoreStages x 8 x 32 float4 of shared memory owned by this warp).
-template <int MT>
+// (kScoreStages x 8 x 32 float4 of shared memory owned by this warp).  `summ`
+// holds one 512-byte row (32 float4) of compressed key per block, of kind KIND.
+template <int MT, int KIND = kSummMean>
 __device__ __forceinline__ void score_warp_range(const uint16_t* __restrict__ q_draft,
-                                                 const float* __restrict__ summ,
+                                                 const float4* __restrict__ summ,
                                                  float* __restrict__ scores, int L, int Hq, int Hkv,
                                                  int G, int NB, int w_lo, int tpw, float4* ring,
                                                  int lane) {
+  static_assert(KIND == kSummMean || MT <= kMaxMinMaxTiles, "min/max row tiles");
   const int g = lane >> 2, t = lane & 3;
   const uint32_t ring_s = smem_u32(ring);
   const int M = L * G;
@@ -124,8 +182,7 @@ __device__ __forceinline__ void score_warp_range(const uint16_t* __restrict__ q_
       const int blk = (tile - u * ntiles) * 8 + g;
       const int st = i % kScoreStages;
       if (blk < NB) {
-        const float4* src = reinterpret_cast<const float4*>(
-                                summ + (static_cast<int64_t>(u) * NB + blk) * kHeadDim) + t;
+        const float4* src = summ + (static_cast<int64_t>(u) * NB + blk) * 32 + t;
 #pragma unroll
         for (int p = 0; p < 8; ++p)
           cp_async16(ring_s + static_cast<uint32_t>(((st * 8 + p) * 32 + lane) * 16), src + 4 * p);
@@ -139,9 +196,10 @@ __device__ __forceinline__ void score_warp_range(const uint16_t* __restrict__ q_
 #pragma unroll
   for (int i = 0; i < kScoreStages - 1; ++i) issue(i);
 
-  // A fragments of unit u: rows 16mt+g (+8), dims 16p+4t..+3, as bf16 pairs
-  // (rows >= L*G are padding and stay zero)
-  uint32_t wq[MT][8][frag_words(MT)];
+  // A fragments of unit u, rows 16mt+g (+8) (rows >= L*G are padding and stay
+  // zero).  Mean: dims 16p+4t..+3 as bf16 pairs.  Min/max: chunk p < 4 holds
+  // q+ of dims 8(t+4p)..+7 and chunk p+4 q- of the same dims.
+  uint32_t wq[MT][8][q_words(MT, KIND)];
   auto load_q = [&](int u) {
     const int b = u / Hkv, h = u - b * Hkv;
 #pragma unroll
@@ -150,19 +208,34 @@ __device__ __forceinline__ void score_warp_range(const uint16_t* __restrict__ q_
       for (int half = 0; half < 2; ++half) {
         const int row = 16 * mt + g + 8 * half;
         const int l = row / G, gq = row - l * G;
-        const uint2* src = reinterpret_cast<const uint2*>(
-            q_draft + ((static_cast<int64_t>(b) * L + l) * Hq + h * G + gq) * kHeadDim + 4 * t);
+        const uint16_t* qrow = q_draft + ((static_cast<int64_t>(b) * L + l) * Hq + h * G + gq) * kHeadDim;
+        if constexpr (KIND == kSummMinMax) {
+          const uint4* src = reinterpret_cast<const uint4*>(qrow + 8 * t);
 #pragma unroll
-        for (int p = 0; p < 8; ++p) {
-          const uint2 w = row < M ? __ldg(src + 4 * p) : make_uint2(0u, 0u);
-          if constexpr (MT == 1) {
-            wq[mt][p][half] = w.x << 16;
-            wq[mt][p][2 + half] = w.x & 0xFFFF0000u;
-            wq[mt][p][4 + half] = w.y << 16;
-            wq[mt][p][6 + half] = w.y & 0xFFFF0000u;
-          } else {
-            wq[mt][p][2 * half] = w.x;
-            wq[mt][p][2 * half + 1] = w.y;
+          for (int p = 0; p < 4; ++p) {
+            const uint4 w = row < M ? __ldg(src + 4 * p) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t neg = ((ws[i] & 0x80008000u) >> 15) * 0xFFFFu;  // negative halves
+              wq[mt][p][4 * half + i] = ws[i] & ~neg;
+              wq[mt][p + 4][4 * half + i] = ws[i] & neg;
+            }
+          }
+        } else {
+          const uint2* src = reinterpret_cast<const uint2*>(qrow + 4 * t);
+#pragma unroll
+          for (int p = 0; p < 8; ++p) {
+            const uint2 w = row < M ? __ldg(src + 4 * p) : make_uint2(0u, 0u);
+            if constexpr (MT == 1) {
+              wq[mt][p][half] = w.x << 16;
+              wq[mt][p][2 + half] = w.x & 0xFFFF0000u;
+              wq[mt][p][4 + half] = w.y << 16;
+              wq[mt][p][6 + half] = w.y & 0xFFFF0000u;
+            } else {
+              wq[mt][p][2 * half] = w.x;
+              wq[mt][p][2 * half + 1] = w.y;
+            }
           }
         }
       }
@@ -185,7 +258,11 @@ __device__ __forceinline__ void score_warp_range(const uint16_t* __restrict__ q_
 #pragma unroll
     for (int p = 0; p < 8; ++p) v[p] = ring[(st * 8 + p) * 32 + lane];
     const int64_t out_off = static_cast<int64_t>(u) * NB;
-    score_tile<MT>(v, wq, lane, g, t, M, (tile - u * ntiles) * 8, NB, out_off, scores + out_off);
+    if constexpr (KIND == kSummMinMax)
+      score_tile_minmax<MT>(v, wq, g, t, M, (tile - u * ntiles) * 8, NB, out_off,
+                            scores + out_off);
+    else
+      score_tile<MT>(v, wq, g, t, M, (tile - u * ntiles) * 8, NB, out_off, scores + out_off);
   }
   cp_async_wait<0>();
 }

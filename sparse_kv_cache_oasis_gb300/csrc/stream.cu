@@ -64,7 +64,8 @@ __global__ void __launch_bounds__(kFusedThreads) attn_score_kernel(
   const int tpw = w_lo + qw < t_hi ? qw : t_hi - w_lo;
   float4* ring = reinterpret_cast<float4*>(smem + (attends ? kAttnSmemBody : 0)) +
                  sw * kScoreStages * 8 * 32;
-  score_warp_range<MT>(q_draft, summ, scores, L, Hq, Hkv, G, NB, w_lo, tpw, ring, lane);
+  score_warp_range<MT>(q_draft, reinterpret_cast<const float4*>(summ), scores, L, Hq, Hkv, G, NB,
+                       w_lo, tpw, ring, lane);
 }
 
 template <int MT>

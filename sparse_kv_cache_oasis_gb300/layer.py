@@ -95,6 +95,14 @@ class LayerState:
         self.fetch_done = torch.cuda.Event()
         self.fetch_done.record(torch.cuda.current_stream(dev))
 
+    def build_minmax_summaries(self):
+        """Min/max compressed keys beside the mean ones: self.summ_mm
+        [B, Hkv, NB, 2, D] bf16 (max row, min row)."""
+        c = self.cfg
+        self.summ_mm = torch.empty((c.batch, c.num_kv_heads, c.num_blocks, 2, c.head_dim),
+                                   dtype=torch.bfloat16, device=self.summ.device)
+        ob.oasis_build_summaries_minmax(c, self.host_k_dev, self.summ_mm)
+
     # -- the five calls -----------------------------------------------------
     def attention(self, q, stream=None):
         ob.oasis_sparse_decode_attn(self.cfg, q, self.pool_k, self.pool_v, self.block_of_slot,
@@ -119,6 +127,10 @@ class LayerState:
         ob.oasis_plan_fetch(self.cfg, self.topk, step, self.slot_of_block, self.block_of_slot,
                             self.last_used, self.fetch_block, self.fetch_slot, self.evict_block,
                             self.n_fetch, self.n_evict, stream)
+
+    def score_minmax(self, q_draft, stream=None):
+        """Scoring against the min/max compressed keys into self.scores."""
+        ob.oasis_score_blocks_minmax(self.cfg, q_draft, self.summ_mm, self.scores, stream)
 
     def predict_clocked(self, q_draft, stream=None):
         """predict() with the step taken from (and advanced in) self.clock."""

@@ -109,6 +109,11 @@ def test_entry_points_reject_bad_arguments_before_launch(lib):
     assert L.oasis_sparse_decode_attn_joint(C.byref(c), ok, odd, ok, ok, ok, null, 0.1, ok, null) == ob.OASIS_ERR_INVALID_ARG
     assert L.oasis_sparse_decode_attn_joint(C.byref(c), ok, ok, ok, ok, ok, null, 0.1, null, null) == ob.OASIS_ERR_INVALID_ARG
     assert L.oasis_sparse_decode_attn_joint(C.byref(c), ok, ok, ok, ok, ok, null, math.inf, ok, null) == ob.OASIS_ERR_INVALID_ARG
+    # min/max scoring: at most 32 query rows per KV head, alignment as for the mean keys
+    wide = ob.OasisConfig.make(dict(W.TINY.config(), lookahead=9))  # L*G = 36
+    assert L.oasis_score_blocks_minmax(C.byref(wide), ok, ok, ok, null) == ob.OASIS_ERR_UNSUPPORTED
+    assert L.oasis_score_blocks_minmax(C.byref(c), odd, ok, ok, null) == ob.OASIS_ERR_INVALID_ARG
+    assert L.oasis_build_summaries_minmax(C.byref(c), ok, odd, null) == ob.OASIS_ERR_INVALID_ARG
     bad = ob.OasisConfig.make(dict(W.TINY.config(), head_dim=64))
     assert L.oasis_score_blocks(C.byref(bad), ok, ok, ok, null) == ob.OASIS_ERR_UNSUPPORTED
     assert L.oasis_select_topk(None, ok, ok, null) == ob.OASIS_ERR_INVALID_ARG

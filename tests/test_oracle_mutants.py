@@ -28,6 +28,12 @@ MUTANTS = {
                                    "(((size_t)b * L + l) * Hq + (size_t)g * H + h) * D"),
     "score draft/batch index swapped": ("(((size_t)b * L + l) * Hq + (size_t)h * G + g) * D",
                                         "(((size_t)l * B + b) * Hq + (size_t)h * G + g) * D"),
+    "min/max summary rows swapped": ("summ_mm[(blk * 2 + 0) * D + d] = hi;", "summ_mm[(blk * 2 + 0) * D + d] = lo;"),
+    "min/max summary skips token 0": ("uint16_t hi = k[(blk * bs) * D + d], lo = hi;",
+                                      "uint16_t hi = k[(blk * bs + 1) * D + d], lo = hi;"),
+    "min/max score takes the lower product": ("bound += lo > hi ? lo : hi;", "bound += lo < hi ? lo : hi;"),
+    "min/max score sums over drafts": ("if (bound > best) best = bound;",
+                                       "best = (best == -INFINITY ? 0.0 : best) + bound;"),
     "top-k ties to higher id": ("    return (a->id > b->id) - (a->id < b->id);\n}\n\n/*\n * Per-KV-head",
                                 "    return (a->id < b->id) - (a->id > b->id);\n}\n\n/*\n * Per-KV-head"),
     "top-k sorts ascending": ("if (a->s > b->s) return -1;\n    if (a->s < b->s) return 1;",

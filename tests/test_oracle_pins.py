@@ -443,6 +443,87 @@ def test_attention_closed_forms_and_masking():
     assert not out.any()
 
 
+# ----------------------------------------------------------------------------
+# min/max compressed keys
+# ----------------------------------------------------------------------------
+def test_minmax_summaries_are_columnwise_extremes():
+    cfg = small_cfg(batch=2, num_q_heads=4, num_kv_heads=2, num_blocks=3, top_k=2)
+    rs = np.random.default_rng(41)
+    k = bf(rs.standard_normal((2, 2, 3, 16, 128)).astype(np.float32))
+    # +0 / -0 ties: block (0,0,0) dim 0 holds -0 first, then +0 (all else positive)
+    k[0, 0, 0, :, 0] = bf(np.full(16, 1.5, np.float32))
+    k[0, 0, 0, 3, 0], k[0, 0, 0, 9, 0] = 0x8000, 0x0000
+    mm = oracle.build_summaries_minmax(cfg, k)
+    kf = f32(k)
+    assert np.array_equal(f32(mm[:, :, :, 0]), kf.max(axis=3))
+    assert np.array_equal(f32(mm[:, :, :, 1]), kf.min(axis=3))
+    assert mm[0, 0, 0, 1, 0] == 0x8000 and mm[0, 0, 0, 0, 0] == bf(1.5)
+    # every stored value is one of the block's own key values (bit for bit)
+    for idx in [(1, 1, 2, 0, 17), (0, 1, 1, 1, 100)]:
+        b, h, j, r, d = idx
+        assert mm[idx] in set(k[b, h, j, :, d].tolist())
+
+
+def test_minmax_score_is_the_box_bound():
+    """sum_d max(q_d mn_d, q_d mx_d) is the largest q.x over the box
+    [mn, mx]: with D = 4 the 16 corners give it by brute force."""
+    cfg = small_cfg(head_dim=4, num_blocks=5, lookahead=3, num_q_heads=2, num_kv_heads=1)
+    rs = np.random.default_rng(42)
+    k = bf(rs.standard_normal((1, 1, 5, 16, 4)).astype(np.float32))
+    qd = bf(rs.standard_normal((1, 3, 2, 4)).astype(np.float32))
+    mm = oracle.build_summaries_minmax(cfg, k)
+    sc = oracle.score_blocks_minmax(cfg, qd, mm)
+    mx, mn = f32(mm[0, 0, :, 0]).astype(np.float64), f32(mm[0, 0, :, 1]).astype(np.float64)
+    q = f32(qd[0]).astype(np.float64).reshape(6, 4)
+    for j in range(5):
+        corners = np.array([[mx[j, d] if (c >> d) & 1 else mn[j, d] for d in range(4)]
+                            for c in range(16)])
+        want = (q @ corners.T).max()
+        assert sc[0, 0, j] == np.float32(want)
+        # an upper bound of every key of the block, for every draft query
+        assert sc[0, 0, j] >= (q @ f32(k[0, 0, j]).astype(np.float64).T).max() - 1e-6
+
+
+def test_minmax_score_closed_forms():
+    cfg = small_cfg(num_blocks=4, lookahead=1, num_q_heads=1, num_kv_heads=1)
+    rs = np.random.default_rng(43)
+    k = bf(rs.standard_normal((1, 1, 4, 16, 128)).astype(np.float32))
+    # block 3: all 16 keys equal -> min = max = the key -> the plain dot product
+    k[0, 0, 3] = k[0, 0, 3, 5]
+    mm = oracle.build_summaries_minmax(cfg, k)
+    kf = f32(k).astype(np.float64)
+    qpos = bf(np.abs(rs.standard_normal((1, 1, 1, 128))).astype(np.float32))
+    qneg = bf(-np.abs(rs.standard_normal((1, 1, 1, 128))).astype(np.float32))
+    qp, qn = f32(qpos[0, 0, 0]).astype(np.float64), f32(qneg[0, 0, 0]).astype(np.float64)
+    sp = oracle.score_blocks_minmax(cfg, qpos, mm)[0, 0]
+    sn = oracle.score_blocks_minmax(cfg, qneg, mm)[0, 0]
+    for j in range(4):
+        assert sp[j] == np.float32(qp @ kf[0, 0, j].max(axis=0))   # q >= 0 picks the max row
+        assert sn[j] == np.float32(qn @ kf[0, 0, j].min(axis=0))   # q <= 0 picks the min row
+    assert sp[3] == np.float32(qp @ kf[0, 0, 3, 0])
+    # a constant block scores as its mean key does (the mean is that key)
+    summ = oracle.build_summaries(cfg, k)
+    assert oracle.score_blocks(cfg, qpos, summ)[0, 0, 3] == sp[3]
+
+
+def test_minmax_score_max_over_drafts_and_group():
+    # the block's score is the best (l, g) bound; head h reads only its own group
+    cfg = small_cfg(num_blocks=3, lookahead=2, num_q_heads=4, num_kv_heads=2, top_k=2)
+    rs = np.random.default_rng(44)
+    k = bf(rs.standard_normal((1, 2, 3, 16, 128)).astype(np.float32))
+    qd = bf(rs.standard_normal((1, 2, 4, 128)).astype(np.float32))
+    mm = oracle.build_summaries_minmax(cfg, k)
+    sc = oracle.score_blocks_minmax(cfg, qd, mm)
+    for h in range(2):
+        single = []
+        for l in range(2):
+            for g in range(2):
+                c1 = small_cfg(num_blocks=3, lookahead=1, num_q_heads=1, num_kv_heads=1, top_k=2)
+                q1 = np.ascontiguousarray(qd[:, l:l + 1, h * 2 + g:h * 2 + g + 1])
+                single.append(oracle.score_blocks_minmax(c1, q1, np.ascontiguousarray(mm[:, h:h + 1]))[0, 0])
+        assert np.array_equal(sc[0, h], np.max(single, axis=0))
+
+
 def test_joint_attention_rows_follow_their_tokens():
     """Joint attention: output row l of request b, head n attends with draft
     token l-1's query (row 0: the decoded token's).  Keys are one-hot per
