@@ -235,6 +235,54 @@ int orc_select_topk(const orc_cfg* c, const float* scores, int32_t* topk_ids)
     return rc;
 }
 
+/*
+ * Top-K over a growing context.  Reading of 'What they did' item 4 (the
+ * local window of recent tokens stays in the working set) once decoding
+ * appends tokens: with n = ceil(ctx_len[b] / bs) blocks in the context (at
+ * most NB), the forced blocks are the sink [0, min(sink, n)) and the last
+ * `local` blocks of the context [max(n - local, 0), n); the other blocks of
+ * the context compete by score, and blocks at or beyond n (not yet written)
+ * rank as if scored -infinity, so they are picked only when the context has
+ * fewer than K blocks.  Ties: lower id first.  With ctx_len = NB * bs this
+ * is orc_select_topk.
+ */
+int orc_select_topk_ctx(const orc_cfg* c, const float* scores, const int32_t* ctx_len,
+                        int32_t* topk_ids)
+{
+    const int B = c->batch, H = c->num_kv_heads, NB = c->num_blocks, K = c->top_k;
+    const int bs = c->block_size;
+    scored_id* rest = (scored_id*)malloc(sizeof(scored_id) * (size_t)NB);
+    int rc = 0;
+    if (!rest) return -2;
+    for (int b = 0; b < B && rc == 0; ++b) {
+        long long nb = ctx_len[b] <= 0 ? 0 : ((long long)ctx_len[b] + bs - 1) / bs;
+        const int n = nb > NB ? NB : (int)nb;
+        const int sink_end = c->sink_blocks < n ? c->sink_blocks : n;
+        const int win_begin = n - c->local_blocks > 0 ? n - c->local_blocks : 0;
+        for (int h = 0; h < H; ++h) {
+            const float* sc = scores + ((size_t)b * H + h) * NB;
+            int32_t* out = topk_ids + ((size_t)b * H + h) * K;
+            int nf = 0, nr = 0;
+            for (int j = 0; j < NB; ++j) {
+                const int forced = j < sink_end || (j >= win_begin && j < n);
+                if (forced) {
+                    if (nf >= K) { rc = -1; break; }
+                    out[nf++] = j;
+                } else {
+                    rest[nr].s = j < n ? sc[j] : -INFINITY;
+                    rest[nr].id = j;
+                    ++nr;
+                }
+            }
+            if (rc) break;
+            qsort(rest, (size_t)nr, sizeof(scored_id), cmp_score_desc_id_asc);
+            for (int i = 0; nf + i < K; ++i) out[nf + i] = rest[i].id;
+        }
+    }
+    free(rest);
+    return rc;
+}
+
 typedef struct { int32_t last; int32_t blk; int32_t slot; } lru_entry;
 
 /* LRU order: least recently used first; equal times by lower block id. */
@@ -399,6 +447,109 @@ int orc_fetch_blocks(const orc_cfg* c, const uint16_t* host_k, const uint16_t* h
             }
         }
     return 0;
+}
+
+/*
+ * Decode-time append (the decode loop of [OasisKV] Fig. 8 advances one token
+ * per step; the page leaves the bookkeeping open, these are the readings):
+ * for each request b the new token sits at position p = ctx_len[b], in block
+ * j = p / bs, row t = p % bs, for every KV head h.
+ *  1. The full cache gets the token: host K/V [b,h,j,t,:] = k_new/v_new [b,h,:].
+ *  2. The working set holds the newest block, so that the token attends to
+ *     itself and to the tokens just before it: if block j is not resident it
+ *     takes a slot now -- the lowest empty slot, else the least recently used
+ *     resident block that is not forced in the grown context (sink and local
+ *     window of n = j + 1 blocks, as in orc_select_topk_ctx), ties by lower
+ *     block id -- with last_used = the step, and rows 0..t-1 of the block are
+ *     copied in from the full cache.  Row t of the slot gets the token.
+ *  3. The block's compressed keys cover its tokens in the context, rows
+ *     0..t: the mean (summed in double in row order, divided by t+1, rounded
+ *     once to fp32) and, if summ_mm is given, the max and min rows.
+ *  4. ctx_len[b] = p + 1.
+ * The step is clock[b*H+h] when clock is given, else `step`.  A request whose
+ * context is full (p >= NB*bs) or negative is left unchanged and the call
+ * returns -1; a head with no slot to give (every resident block forced, none
+ * empty) gets rows 1 and 3 only and the call returns -2.  Returns 0 otherwise.
+ */
+int orc_append_kv(const orc_cfg* c, const uint16_t* k_new, const uint16_t* v_new,
+                  int32_t* ctx_len, const int32_t* clock, int32_t step, uint16_t* host_k,
+                  uint16_t* host_v, int32_t* slot_of_block, int32_t* block_of_slot,
+                  int32_t* last_used, uint16_t* pool_k, uint16_t* pool_v, float* summ,
+                  uint16_t* summ_mm)
+{
+    const int B = c->batch, H = c->num_kv_heads, NB = c->num_blocks;
+    const int bs = c->block_size, D = c->head_dim, S = slots_of(c);
+    int rc = 0;
+    for (int b = 0; b < B; ++b) {
+        const int32_t p = ctx_len[b];
+        if (p < 0 || (long long)p >= (long long)NB * bs) { rc = -1; continue; }
+        const int j = p / bs, t = p % bs;
+        const int n = j + 1;
+        const int sink_end = c->sink_blocks < n ? c->sink_blocks : n;
+        const int win_begin = n - c->local_blocks > 0 ? n - c->local_blocks : 0;
+        for (int h = 0; h < H; ++h) {
+            const size_t u = (size_t)b * H + h;
+            const size_t row = ((u * NB + j) * bs + t) * D;
+            int32_t* sob = slot_of_block + u * NB;
+            int32_t* bos = block_of_slot + u * S;
+            int32_t* lu = last_used + u * S;
+            /* 1 */
+            memcpy(host_k + row, k_new + u * D, sizeof(uint16_t) * D);
+            memcpy(host_v + row, v_new + u * D, sizeof(uint16_t) * D);
+            /* 2 */
+            int32_t s = sob[j];
+            if (s < 0) {
+                int best = -1;
+                for (int q = 0; q < S && best < 0; ++q)
+                    if (bos[q] < 0) best = q;
+                if (best < 0)
+                    for (int q = 0; q < S; ++q) {
+                        const int32_t blk = bos[q];
+                        if (blk < sink_end || (blk >= win_begin && blk < n)) continue;
+                        if (best < 0 || lu[q] < lu[best] || (lu[q] == lu[best] && blk < bos[best]))
+                            best = q;
+                    }
+                if (best < 0) {
+                    rc = rc ? rc : -2;
+                } else {
+                    if (bos[best] >= 0) sob[bos[best]] = -1;
+                    bos[best] = j;
+                    sob[j] = best;
+                    lu[best] = clock ? clock[u] : step;
+                    s = best;
+                    for (int r = 0; r < t; ++r) {
+                        memcpy(pool_k + ((u * S + s) * bs + r) * D, host_k + ((u * NB + j) * bs + r) * D,
+                               sizeof(uint16_t) * D);
+                        memcpy(pool_v + ((u * S + s) * bs + r) * D, host_v + ((u * NB + j) * bs + r) * D,
+                               sizeof(uint16_t) * D);
+                    }
+                }
+            }
+            if (s >= 0) {
+                memcpy(pool_k + ((u * S + s) * bs + t) * D, k_new + u * D, sizeof(uint16_t) * D);
+                memcpy(pool_v + ((u * S + s) * bs + t) * D, v_new + u * D, sizeof(uint16_t) * D);
+            }
+            /* 3 */
+            for (int d = 0; d < D; ++d) {
+                const uint16_t* kb = host_k + (u * NB + j) * bs * D + d;
+                double sum = 0.0;
+                uint16_t hi = kb[0], lo = kb[0];
+                for (int r = 0; r <= t; ++r) {
+                    sum += bf16_to_double(kb[(size_t)r * D]);
+                    if (bf16_to_double(kb[(size_t)r * D]) > bf16_to_double(hi)) hi = kb[(size_t)r * D];
+                    if (bf16_to_double(kb[(size_t)r * D]) < bf16_to_double(lo)) lo = kb[(size_t)r * D];
+                }
+                summ[(u * NB + j) * D + d] = (float)(sum / (double)(t + 1));
+                if (summ_mm) {
+                    summ_mm[((u * NB + j) * 2 + 0) * D + d] = hi;
+                    summ_mm[((u * NB + j) * 2 + 1) * D + d] = lo;
+                }
+            }
+        }
+        /* 4 */
+        ctx_len[b] = p + 1;
+    }
+    return rc;
 }
 
 /*

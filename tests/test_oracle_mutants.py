@@ -34,6 +34,14 @@ MUTANTS = {
     "min/max score takes the lower product": ("bound += lo > hi ? lo : hi;", "bound += lo < hi ? lo : hi;"),
     "min/max score sums over drafts": ("if (bound > best) best = bound;",
                                        "best = (best == -INFINITY ? 0.0 : best) + bound;"),
+    "ctx top-K window at the end of the capacity": (
+        "const int win_begin = n - c->local_blocks > 0 ? n - c->local_blocks : 0;",
+        "const int win_begin = NB - c->local_blocks > 0 ? NB - c->local_blocks : 0;"),
+    "ctx top-K keeps scores past the context": ("rest[nr].s = j < n ? sc[j] : -INFINITY;", "rest[nr].s = sc[j];"),
+    "append summary divides by bs": ("(float)(sum / (double)(t + 1))", "(float)(sum / (double)bs)"),
+    "append evicts the most recent": ("lu[q] < lu[best] || (lu[q] == lu[best]", "lu[q] > lu[best] || (lu[q] == lu[best]"),
+    "append skips the earlier rows": ("for (int r = 0; r < t; ++r) {", "for (int r = 0; r < 0; ++r) {"),
+    "append keeps the context length": ("ctx_len[b] = p + 1;", "ctx_len[b] = p;"),
     "top-k ties to higher id": ("    return (a->id > b->id) - (a->id < b->id);\n}\n\n/*\n * Per-KV-head",
                                 "    return (a->id < b->id) - (a->id > b->id);\n}\n\n/*\n * Per-KV-head"),
     "top-k sorts ascending": ("if (a->s > b->s) return -1;\n    if (a->s < b->s) return 1;",

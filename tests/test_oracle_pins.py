@@ -524,6 +524,108 @@ def test_minmax_score_max_over_drafts_and_group():
         assert np.array_equal(sc[0, h], np.max(single, axis=0))
 
 
+# ----------------------------------------------------------------------------
+# growing context: top-K with a sliding local window, and the append
+# ----------------------------------------------------------------------------
+def test_topk_ctx_hand_cases():
+    # NB = 8, K = 4, sink 1, local 2; scores favour high ids except block 1
+    cfg = small_cfg(num_blocks=8, kv_budget_tokens=16 * 4, top_k=4, sink_blocks=1, local_blocks=2)
+    sc = np.asarray([[[0.1, 5.0, 0.2, 0.3, 7.0, 8.0, 9.0, 10.0]]], np.float32)
+    def ids(ctx):
+        return oracle.select_topk_ctx(cfg, sc, np.asarray([ctx], np.int32))[0, 0].tolist()
+    assert ids(50) == [0, 2, 3, 1]        # 4 blocks: sink 0, window {2, 3}, then block 1 by score
+    assert ids(17) == [0, 1, 2, 3]        # 2 blocks, both forced; the rest rank -inf -> lowest ids
+    assert ids(0) == [0, 1, 2, 3]         # empty context: nothing forced, all -inf
+    assert ids(16 * 5) == [0, 3, 4, 1]    # 5 blocks: window {3, 4}; block 1 beats block 2
+    assert ids(16 * 8) == [0, 6, 7, 5]    # full context: as the plain top-K
+    assert ids(16 * 8) == oracle.select_topk(cfg, sc)[0, 0].tolist()
+
+
+def test_topk_ctx_full_context_is_plain_topk():
+    cfg = small_cfg(batch=2, num_q_heads=4, num_kv_heads=2, num_blocks=40, kv_budget_tokens=16 * 12,
+                    top_k=12, sink_blocks=2, local_blocks=3)
+    sc = np.random.default_rng(45).standard_normal((2, 2, 40)).astype(np.float32)
+    full = np.asarray([40 * 16, 40 * 16], np.int32)
+    assert np.array_equal(oracle.select_topk_ctx(cfg, sc, full), oracle.select_topk(cfg, sc))
+
+
+def _append_setup():
+    B, H, NB, S = 2, 2, 6, 3
+    cfg = small_cfg(batch=B, num_q_heads=H, num_kv_heads=H, num_blocks=NB, kv_budget_tokens=16 * S,
+                    top_k=3, sink_blocks=1, local_blocks=1)
+    rs = np.random.default_rng(46)
+    hk = bf(rs.standard_normal((B, H, NB, 16, 128)).astype(np.float32))
+    hv = bf(rs.standard_normal((B, H, NB, 16, 128)).astype(np.float32))
+    kn = bf(rs.standard_normal((B, H, 128)).astype(np.float32))
+    vn = bf(rs.standard_normal((B, H, 128)).astype(np.float32))
+    bos = np.asarray([[[0, 1, -1], [0, 3, 1]], [[0, 2, 4], [0, 4, 5]]], np.int32)
+    lu = np.asarray([[[4, 4, -1], [5, 2, 2]], [[1, 1, 1], [1, 3, 0]]], np.int32)
+    sob = np.full((B, H, NB), -1, np.int32)
+    for b in range(B):
+        for h in range(H):
+            for q in range(S):
+                if bos[b, h, q] >= 0:
+                    sob[b, h, bos[b, h, q]] = q
+    pk = bf(rs.standard_normal((B, H, S, 16, 128)).astype(np.float32))
+    pv = bf(rs.standard_normal((B, H, S, 16, 128)).astype(np.float32))
+    summ = rs.standard_normal((B, H, NB, 128)).astype(np.float32)
+    mm = bf(rs.standard_normal((B, H, NB, 2, 128)).astype(np.float32))
+    return cfg, hk, hv, kn, vn, sob, bos, lu, pk, pv, summ, mm
+
+
+def test_append_writes_token_summary_and_working_set():
+    cfg, hk, hv, kn, vn, sob, bos, lu, pk, pv, summ, mm = _append_setup()
+    hk0, pk0, pv0 = hk.copy(), pk.copy(), pv.copy()
+    ctx = np.asarray([32, 40], np.int32)       # request 0 starts block 2; request 1 is at row 8 of it
+    rc = oracle.append_kv(cfg, kn, vn, ctx, 9, hk, hv, sob, bos, lu, pk, pv, summ, mm)
+    assert rc == 0 and ctx.tolist() == [33, 41]
+    for b, t in ((0, 0), (1, 8)):
+        for h in range(2):
+            assert np.array_equal(hk[b, h, 2, t], kn[b, h]) and np.array_equal(hv[b, h, 2, t], vn[b, h])
+            rows = f32(hk[b, h, 2, :t + 1]).astype(np.float64)
+            assert np.array_equal(summ[b, h, 2], np.float32([math.fsum(c) / (t + 1) for c in rows.T]))
+            assert np.array_equal(f32(mm[b, h, 2, 0]), rows.max(0).astype(np.float32))
+            assert np.array_equal(f32(mm[b, h, 2, 1]), rows.min(0).astype(np.float32))
+    # (0,0): empty slot 2 takes block 2
+    assert bos[0, 0].tolist() == [0, 1, 2] and sob[0, 0, 2] == 2 and lu[0, 0, 2] == 9
+    # (0,1): no empty slot; blocks 3 and 1 tie at last use 2 -> block 1 (lower id) leaves slot 2
+    assert bos[0, 1].tolist() == [0, 3, 2] and sob[0, 1, 1] == -1 and lu[0, 1].tolist() == [5, 2, 9]
+    # (1,0): block 2 already resident in slot 1 -> only row 8 of slot 1 changes
+    assert bos[1, 0].tolist() == [0, 2, 4] and lu[1, 0].tolist() == [1, 1, 1]
+    assert np.array_equal(pk[1, 0, 1, 8], kn[1, 0])
+    changed = np.argwhere((pk[1, 0] != pk0[1, 0]).any(axis=-1))
+    assert changed.tolist() == [[1, 8]]
+    # (1,1): LRU block 5 (last use 0) leaves slot 2; rows 0-7 of block 2 come in from the cache
+    assert bos[1, 1].tolist() == [0, 4, 2] and sob[1, 1, 5] == -1 and lu[1, 1, 2] == 9
+    assert np.array_equal(pk[1, 1, 2, :8], hk0[1, 1, 2, :8]) and np.array_equal(pk[1, 1, 2, 8], kn[1, 1])
+    assert np.array_equal(pk[1, 1, 2, 9:], pk0[1, 1, 2, 9:])      # rows past the context untouched
+    # blocks other than 2 keep their summaries and cache rows
+    assert np.array_equal(np.delete(hk, 2, axis=2), np.delete(hk0, 2, axis=2))
+
+
+def test_append_full_context_and_no_free_slot():
+    cfg, hk, hv, kn, vn, sob, bos, lu, pk, pv, summ, mm = _append_setup()
+    full = dict(cfg, local_blocks=3)   # window of 3 blocks: every resident block of (0,1) is forced
+    ctx = np.asarray([16 * 6, 16 * 4], np.int32)   # request 0 full; request 1 starts block 4
+    bos[1, 1] = [0, 2, 3]
+    lu[1, 1] = [0, 0, 0]
+    sob[1, 1] = -1
+    sob[1, 1, 0], sob[1, 1, 2], sob[1, 1, 3] = 0, 1, 2
+    hk0, pk0, bos0, sob0 = hk.copy(), pk.copy(), bos.copy(), sob.copy()
+    rc = oracle.append_kv(full, kn, vn, ctx, 3, hk, hv, sob, bos, lu, pk, pv, summ, mm)
+    assert rc == -1 and ctx.tolist() == [96, 65]
+    assert np.array_equal(hk[0], hk0[0]) and np.array_equal(pk[0], pk0[0])   # request 0 untouched
+    # (1,1): blocks 0 (sink), 2 and 3 (window of block 4) are forced: no slot, pool untouched
+    assert np.array_equal(bos[1, 1], bos0[1, 1]) and np.array_equal(pk[1, 1], pk0[1, 1])
+    assert np.array_equal(hk[1, 1, 4, 0], kn[1, 1])
+    assert np.array_equal(summ[1, 1, 4], f32(kn[1, 1]))
+    # (1,0): block 4 resident in slot 2 -> row 0 written there
+    assert np.array_equal(pk[1, 0, 2, 0], kn[1, 0])
+    rc = oracle.append_kv(full, kn, vn, np.asarray([5, 70], np.int32), 3, hk, hv, sob, bos, lu, pk, pv,
+                          summ, mm)
+    assert rc == -2
+
+
 def test_joint_attention_rows_follow_their_tokens():
     """Joint attention: output row l of request b, head n attends with draft
     token l-1's query (row 0: the decoded token's).  Keys are one-hot per
