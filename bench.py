@@ -46,6 +46,7 @@ UNIT = "tok/s"
 WORKLOAD = W.LLAMA8B_LAYER
 INSTANCES = 4
 QUERY_SETS = 20          # the workload's 20 consecutive decode steps, cycled
+GROW_ROOM = 1024         # tokens of room left in each context for the growing-context run
 
 
 def parse():
@@ -58,6 +59,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-grow", action="store_true", help="skip the growing-context run")
+    ap.add_argument("--profile-grow", action="store_true",
+                    help="with --profile-steps: run the growing-context form of the step")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="only run this many untimed graph steps (for ncu launch lists)")
     ap.add_argument("--profile-joint", type=int, default=0,
@@ -341,6 +345,29 @@ def committed_traffic(kernel: str):
         return None
 
 
+_uploaded = set()
+
+
+def upload_graph(g, stream):
+    """Uploads an instantiated CUDA graph to the device ahead of its first
+    launch (driver cuGraphUpload on the graph's executable), once per graph;
+    a no-op where the executable is not exposed."""
+    import ctypes
+    get = getattr(g, "raw_cuda_graph_exec", None)
+    if get is None or id(g) in _uploaded:
+        return
+    try:
+        exe = get()
+        drv = ctypes.CDLL("libcuda.so.1")
+        drv.cuGraphUpload.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+        drv.cuGraphUpload.restype = ctypes.c_int
+        rc = drv.cuGraphUpload(ctypes.c_void_p(exe), ctypes.c_void_p(stream.cuda_stream))
+        if rc == 0:
+            _uploaded.add(id(g))
+    except Exception:
+        pass
+
+
 def gpu_arm(args):
     import torch
     import torch.distributed as dist
@@ -388,7 +415,14 @@ def gpu_arm(args):
     copy = torch.cuda.Stream(device=dev, priority=-1)
     h2d = torch.cuda.Stream(device=dev)
     d2h = torch.cuda.Stream(device=dev)
+    side = torch.cuda.Stream(device=dev)
     out_host = [torch.empty_like(L.out, device="cpu").pin_memory() for L in layers]
+    # the decoded token's K and V rows per layer copy, for the growing-context run
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(wl.seed + 7)
+    kv_new = [tuple((torch.randn((wl.batch, wl.num_kv_heads, wl.head_dim), generator=gen,
+                                 device=dev) * 0.5).to(torch.bfloat16) for _ in range(2))
+              for _ in range(n_inst)]
     qq_in = [torch.empty_like(qq_host[i][0], device=dev) for i in range(n_inst)]
     nq = q_dev[0][0].numel()
     q_in = [qq_in[i][:nq].view(q_dev[i][0].shape) for i in range(n_inst)]
@@ -397,7 +431,7 @@ def gpu_arm(args):
     def qset(s):
         return s % n_inst, (s // n_inst) % QUERY_SETS
 
-    def enqueue(s, active, host_io: bool):
+    def enqueue(s, active, host_io: bool, grow: bool = False):
         """Graph body of step s, a software pipeline over the layer copies as in
         Fig. 8 (each layer's prediction and transfer run in the background of
         the following layers): the attention of step s and the scoring of step
@@ -408,7 +442,9 @@ def gpu_arm(args):
         produced by an earlier graph.  With host I/O, step s+1's queries are
         copied in from pinned host memory and step s-1's output is copied out
         beside step s's kernels (a run's first step copies its own queries in
-        before its attention)."""
+        before its attention).  With `grow`, step s first appends its token to
+        its layer copy (cache, working set, summaries, context length) and the
+        selection uses the window at each context's end."""
         fork = torch.cuda.Event()
         fork.record(compute)
         joins = []
@@ -434,6 +470,17 @@ def gpu_arm(args):
         if "attn" in active:
             i, qi = qset(s)
             L = layers[i]
+            if grow:
+                L.append(kv_new[i][0], kv_new[i][1], compute)
+                # the newest block's summaries beside the attention; needed by
+                # this copy's scoring in the next step
+                appended = torch.cuda.Event()
+                appended.record(compute)
+                side.wait_event(appended)
+                L.refresh_summaries(side)
+                refreshed = torch.cuda.Event()
+                refreshed.record(side)
+                joins.append(refreshed)
             q = q_in[i] if host_io else q_dev[i][qi]
             if fused:
                 i1, qi1 = qset(s - 1)
@@ -446,7 +493,10 @@ def gpu_arm(args):
             qd = qd_in[i1] if host_io else qd_dev[i1][qi1]
             L1 = layers[i1]
             branch(score_st, lambda st: ob.oasis_score_blocks(L1.cfg, qd, L1.summ, L1.scores, st))
-        if "select" in active:
+        if "select" in active and grow:
+            L2 = layers[(s - 2) % n_inst]
+            branch(select_st, lambda st: L2.select_ctx(st))
+        elif "select" in active:
             L2 = layers[(s - 2) % n_inst]
             branch(select_st, lambda st: ob.oasis_predict_select(
                 L2.cfg, L2.scores, 0, L2.clock, L2.topk, L2.slot_of_block, L2.block_of_slot,
@@ -489,12 +539,12 @@ def gpu_arm(args):
     period = n_inst * QUERY_SETS
     graphs = {}
 
-    def graph_for(s, active, host_io):
-        key = (s % period, active, host_io)
+    def graph_for(s, active, host_io, grow=False):
+        key = (s % period, active, host_io, grow)
         if key not in graphs:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=compute):
-                enqueue(s, active, host_io)
+                enqueue(s, active, host_io, grow)
             graphs[key] = g
         return graphs[key]
 
@@ -508,17 +558,17 @@ def gpu_arm(args):
         return frozenset(("attn", "score", "select", "fetch")
                          + (("h2d_next", "d2h_prev") if host_io else ()))
 
-    def chunk_graph(s, host_io):
-        key = ("chunk", s % period, host_io)
+    def chunk_graph(s, host_io, grow=False):
+        key = ("chunk", s % period, host_io, grow)
         if key not in graphs:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=compute):
                 for k in range(CHUNK):
-                    enqueue(s + k, full_mask(host_io), host_io)
+                    enqueue(s + k, full_mask(host_io), host_io, grow)
             graphs[key] = g
         return graphs[key]
 
-    def run_steps(s0, n, host_io=False):
+    def run_steps(s0, n, host_io=False, grow=False):
         """Exactly the work of layer-steps s0..s0+n-1 (the pipeline fills in
         the first three graph steps and drains in the last three)."""
         end = s0 + n + 3
@@ -528,23 +578,35 @@ def gpu_arm(args):
             while s < end:
                 if s + CHUNK <= end and all(active_of(s + k, s0, n, host_io) == full
                                             for k in range(CHUNK)):
-                    chunk_graph(s, host_io).replay()
+                    chunk_graph(s, host_io, grow).replay()
                     s += CHUNK
                 else:
-                    graph_for(s, active_of(s, s0, n, host_io), host_io).replay()
+                    graph_for(s, active_of(s, s0, n, host_io), host_io, grow).replay()
                     s += 1
 
-    # capture every graph the long runs below need, outside the timed regions
-    for io in ((False,) if args.no_e2e else (False, True)):
-        masks = {active_of(s, 100, 50, io) for s in range(100, 153)}
-        for s in range(period):
-            for m in masks:
-                graph_for(s, m, io)
-            chunk_graph(s, io)
-    torch.cuda.synchronize()
+    # capture every graph the long runs below need, outside the timed regions,
+    # and upload each to the device (a graph's first launch otherwise pays for
+    # its upload, ~ms for a 16-step graph, inside whichever run launches it first)
+    def capture_all(grow):
+        for io in ((False,) if (args.no_e2e or grow) else (False, True)):
+            masks = {active_of(s_, 100, 50, io) for s_ in range(100, 153)}
+            for s_ in range(period):
+                for m in masks:
+                    graph_for(s_, m, io, grow)
+                chunk_graph(s_, io, grow)
+        for g_ in graphs.values():
+            upload_graph(g_, compute)
+        torch.cuda.synchronize()
+
+    capture_all(False)
 
     if args.profile_steps:
-        run_steps(0, args.profile_steps)
+        if args.profile_grow:  # the growing-context form of the step
+            for L in layers:
+                L.ctx_len = torch.full((wl.batch,), wl.ctx_tokens - GROW_ROOM, dtype=torch.int32,
+                                       device=dev)
+                L.cfg.local_blocks = max(L.cfg.local_blocks, 1)
+        run_steps(0, args.profile_steps, grow=args.profile_grow)
         for r in range(args.profile_joint):  # joint attention launches after the steps
             layers[r % n_inst].attention_joint(q_dev[r % n_inst][0], qd_dev[r % n_inst][0], compute)
         if args.profile_minmax:
@@ -676,6 +738,13 @@ def gpu_arm(args):
     # ---- end to end: inputs copied in from pinned host, output read back, every step
     e2e = None
     if not args.no_e2e:
+        # its own untimed warm-up, one period of the query sets: the host-I/O
+        # graphs' first launches and the device's first touch of every pinned
+        # input buffer (measured: 512 timed steps after 16 warm-up steps ran
+        # at 49 us per step, 10,000 at 33 us)
+        n_warm = max(args.warmup, period + 4 * n_inst)
+        run_steps(s, n_warm, host_io=True)
+        s += n_warm
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
@@ -693,6 +762,63 @@ def gpu_arm(args):
         e2e = {"value": job_throughput(world, wl.batch, ems / n_e2e), "unit": UNIT,
                "h2d_bytes_per_step": q_bytes, "d2h_bytes_per_step": out_host[0].numel() * 2,
                "wall_s": wall}
+
+    # ---- growing context: the same pipelined step with each step's token
+    # appended first (cache, working set, summaries, context length) and the
+    # selection's local window following the context (device-timed, like value)
+    grow = None
+    if not args.no_grow:
+        ctx0 = wl.ctx_tokens - GROW_ROOM
+        for L in layers:
+            L.ctx_len = torch.full((wl.batch,), ctx0, dtype=torch.int32, device=dev)
+            # a local window of at least the newest block, so that the planner
+            # keeps the block the appends write into resident
+            L.cfg.local_blocks = max(L.cfg.local_blocks, 1)
+        capture_all(True)
+        n_warm = max(args.warmup, period + 4 * n_inst)  # every chunk graph of the run once
+        run_steps(s, n_warm, grow=True)
+        s += n_warm
+        n_grow = min(args.steps, GROW_ROOM * n_inst // 2 - n_warm)
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(compute)
+        run_steps(s, n_grow, grow=True)
+        g1.record(compute)
+        torch.cuda.synchronize()
+        s += n_grow
+        gms = max_over_ranks(g0.elapsed_time(g1), world, dev) / n_grow
+        # the append and refresh kernels alone: graphs of 8 launches over the copies
+        def time_graph(fn):
+            gx = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gx, stream=compute):
+                for r in range(8):
+                    fn(layers[r % n_inst], r % n_inst)
+            vals = []
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(compute)
+                with torch.cuda.stream(compute):
+                    gx.replay()
+                b.record(compute)
+                torch.cuda.synchronize()
+                vals.append(a.elapsed_time(b) / 8)
+            return statistics.mean(vals)
+        append_ms = time_graph(lambda L, i: L.append(kv_new[i][0], kv_new[i][1], compute))
+        refresh_ms = time_graph(lambda L, i: L.refresh_summaries(compute))
+        ctx_end = [int(L.ctx_len.max().item()) for L in layers]
+        gf = []
+        for r in range(n_inst * 4):  # transfer volume over further (untimed) steps
+            run_steps(s, 1, grow=True)
+            s += 1
+            torch.cuda.synchronize()
+            gf.append(int(layers[(s - 1) % n_inst].n_fetch.sum().item()))
+        grow = {"ms_per_step": gms, "value": job_throughput(world, wl.batch, gms), "unit": UNIT,
+                "vs_fixed_context_step": gms / ms_per_step, "append_ms_per_launch": append_ms,
+                "refresh_ms_per_launch": refresh_ms, "fetched_blocks_per_step": statistics.mean(gf),
+                "ctx_start": ctx0, "ctx_end_per_copy": ctx_end, "steps": n_grow,
+                "local_blocks": layers[0].cfg.local_blocks,
+                "kernels": "append_kernel, then attn_score_kernel beside refresh_kernel; "
+                           "topk_plan_kernel with the window at each context's end; fetch_kernel"}
 
     errs = ob.oasis_device_errors()
     cpu = cpu_all = None
@@ -737,6 +863,7 @@ def gpu_arm(args):
                 "achieved_gbs": by["score_mm"] / (mean_ms["score_mm"] * 1e-3) / 1e9,
                 "frac_of_measured_hbm": by["score_mm"] / (mean_ms["score_mm"] * 1e-3) / 1e9 / peak,
                 "vs_mean_scoring": mean_ms["score_mm"] / mean_ms["score"]},
+            "growing_context": grow,
             "kernels_ms": mean_ms,
             "kernel_gbs": {k: by[k] / (mean_ms[k] * 1e-3) / 1e9 for k in kinds},
             "gpu_launches": args.steps * 4,

@@ -17,6 +17,8 @@
  *   oasis_select_topk          top-K blocks per KV head            (diagram step 2)
  *   oasis_plan_fetch           diff vs. working set, capped LRU    (diagram step 3, Tab. 2)
  *   oasis_fetch_blocks         host -> HBM transfer, copy stream   (diagram step 4, Fig. 8)
+ *   oasis_append_kv            the decoded token joins cache and working set (Fig. 8)
+ *   oasis_refresh_summaries    the newest block's compressed keys follow (Fig. 7 left)
  *
  * Conventions
  *   - All pointers except `cfg` and the outputs of the query functions are
@@ -81,6 +83,8 @@ typedef enum {
 #define OASIS_DEVERR_TOPK_IDS     0x4u  /* top-K id out of range or repeated; (b,h) left unchanged */
 #define OASIS_DEVERR_WAIT_TIMEOUT 0x8u  /* a bounded device wait gave up; outputs invalid */
 #define OASIS_DEVERR_SLOT_RANGE   0x10u /* block_of_slot entry >= NB; slot skipped */
+#define OASIS_DEVERR_CTX_FULL     0x20u /* append: context at capacity (NB*bs) or negative; request skipped */
+#define OASIS_DEVERR_NO_SLOT      0x40u /* append: newest block not resident and every slot forced; pool not written */
 
 /* Per-layer problem description ([OasisKV] diagram steps 2-3, Tab. 1-2):
  * block size, KV budget, look-ahead tokens, top-K and fetch ratio. */
@@ -159,6 +163,16 @@ oasis_status_t oasis_score_blocks_minmax(const oasis_config_t* cfg, const uint16
 oasis_status_t oasis_select_topk(const oasis_config_t* cfg, const float* scores,
                                  int32_t* topk_ids, void* stream);
 
+/* Top-K over a growing context ([OasisKV] 'What they did' item 4 as decoding
+ * appends tokens): as oasis_select_topk, with n = ceil(ctx_len[b] / bs) (at
+ * most NB) blocks in request b's context: the forced blocks are the sink
+ * [0, min(sink, n)) and the local window [max(n - local, 0), n), and blocks
+ * at or beyond n rank as if scored -infinity (picked, lowest id first, only
+ * when the context has fewer than K blocks).  ctx_len [B] int32 on the device.
+ * With ctx_len[b] = NB*bs for every b the result is oasis_select_topk's. */
+oasis_status_t oasis_select_topk_ctx(const oasis_config_t* cfg, const float* scores,
+                                     const int32_t* ctx_len, int32_t* topk_ids, void* stream);
+
 /* Selection with capped eviction ([OasisKV] diagram step 3; Tab. 2 "LRU
  * eviction"; Fig. 9 head-wise block map).  Per (b,h), with P = topk_ids and R
  * the resident blocks:
@@ -203,6 +217,60 @@ oasis_status_t oasis_predict_select(const oasis_config_t* cfg, const float* scor
                                     int32_t* last_used, int32_t* fetch_block,
                                     int32_t* fetch_slot, int32_t* evict_block,
                                     int32_t* n_fetch, int32_t* n_evict, void* stream);
+
+/* oasis_predict_select with the top-K of oasis_select_topk_ctx (the window
+ * follows each request's context length ctx_len [B]). */
+oasis_status_t oasis_predict_select_ctx(const oasis_config_t* cfg, const float* scores,
+                                        const int32_t* ctx_len, int32_t step, int32_t* clock,
+                                        int32_t* topk_ids, int32_t* slot_of_block,
+                                        int32_t* block_of_slot, int32_t* last_used,
+                                        int32_t* fetch_block, int32_t* fetch_slot,
+                                        int32_t* evict_block, int32_t* n_fetch, int32_t* n_evict,
+                                        void* stream);
+
+/* Decode-time append ([OasisKV] Fig. 8: the decode loop advances a token per
+ * step) of one token per request, at position p = ctx_len[b] (row t = p % bs
+ * of block j = p / bs), for every KV head h:
+ *   1. host K/V [b,h,j,t,:] = k_new/v_new [b,h,:] (host_k/host_v: mapped
+ *      pinned memory, their device addresses);
+ *   2. the working set holds the newest block: if block j is not resident it
+ *      takes the lowest empty slot, else the slot of the least recently used
+ *      resident block that is not forced in the grown context (sink and
+ *      local window of j + 1 blocks), ties by lower block id; the maps are
+ *      updated, last_used = clock[b*Hkv+h] (clock given) or `step`, and rows
+ *      0..t-1 are copied in from the host cache.  Row t of the slot gets the
+ *      token;
+ *   3. ctx_len[b] = p + 1.
+ * The block's compressed keys follow with oasis_refresh_summaries, which may
+ * run on another stream beside the attention.  k_new, v_new [B][Hkv][D] bf16
+ * (8-byte aligned); ctx_len [B] int32, read and advanced on the device.  A
+ * request whose context is at capacity (p >= NB*bs) is skipped and flags
+ * OASIS_DEVERR_CTX_FULL.  A head whose newest block finds no slot (every
+ * resident block forced) would write the cache only and flag
+ * OASIS_DEVERR_NO_SLOT; with a valid configuration this cannot happen (at
+ * most K <= S forced blocks, the newest one among them), so the flag marks a
+ * broken working set.  Hkv <= 32.  Order it after the step's reads of the
+ * same slots (attention) and before the next planning of the same layer. */
+oasis_status_t oasis_append_kv(const oasis_config_t* cfg, const uint16_t* k_new,
+                               const uint16_t* v_new, int32_t* ctx_len, const int32_t* clock,
+                               int32_t step, uint16_t* host_k, uint16_t* host_v,
+                               int32_t* slot_of_block, int32_t* block_of_slot, int32_t* last_used,
+                               uint16_t* pool_k, uint16_t* pool_v, void* stream);
+
+/* Compressed keys of each context's newest block over its rows inside the
+ * context ([OasisKV] Fig. 7 left, as the context grows): with p = ctx_len[b]
+ * - 1 (nothing for an empty context), block j = p / bs, rows 0..t, t = p % bs:
+ *   summ[b,h,j,:]   = fp32 mean of the rows (double sum in row order,
+ *                     divided by t+1, rounded once), for every KV head h;
+ *   summ_mm         (may be NULL) their max and min rows, bf16.
+ * For a full block this equals oasis_build_summaries(_minmax).  The rows are
+ * read from the working set when the block is resident (pool_k), else from
+ * the host cache; the two hold the same keys.  Call after oasis_append_kv
+ * (ordered after it), before the layer's next scoring. */
+oasis_status_t oasis_refresh_summaries(const oasis_config_t* cfg, const int32_t* ctx_len,
+                                       const uint16_t* host_k, const int32_t* slot_of_block,
+                                       const uint16_t* pool_k, float* summ, uint16_t* summ_mm,
+                                       void* stream);
 
 /* KV transfer ([OasisKV] diagram step 4, Fig. 8): for every r < n_fetch[b,h],
  * copies block fetch_block[b,h,r] of host K and V into slot fetch_slot[b,h,r]

@@ -64,7 +64,8 @@ def lib():
                 "orc_score_blocks_minmax": (None, [cfgp, P, P, P]),
                 "orc_select_topk": (C.c_int, [cfgp, P, P]),
                 "orc_select_topk_ctx": (C.c_int, [cfgp, P, P, P]),
-                "orc_append_kv": (C.c_int, [cfgp, P, P, P, P, C.c_int32, P, P, P, P, P, P, P, P, P]),
+                "orc_append_kv": (C.c_int, [cfgp, P, P, P, P, C.c_int32, P, P, P, P, P, P, P]),
+                "orc_refresh_summaries": (None, [cfgp, P, P, P, P]),
                 "orc_plan_fetch": (C.c_int, [cfgp, P, C.c_int32, P, P, P, P, P, P, P, P]),
                 "orc_fetch_blocks": (C.c_int, [cfgp, P, P, P, P, P, P, P]),
                 "orc_sparse_decode_attn": (None, [cfgp, P, P, P, P, P, C.c_double, P]),
@@ -197,10 +198,10 @@ def select_topk_ctx(cfg: dict, scores: np.ndarray, ctx_len: np.ndarray) -> np.nd
 
 
 def append_kv(cfg: dict, k_new, v_new, ctx_len, step, host_k, host_v, slot_of_block,
-              block_of_slot, last_used, pool_k, pool_v, summ, summ_mm=None, clock=None) -> int:
+              block_of_slot, last_used, pool_k, pool_v, clock=None) -> int:
     """Appends one token per request, in place on every array passed (ctx_len
     included).  Returns the oracle's code: 0, -1 (a full context) or -2 (a
-    head with no slot to give)."""
+    head with no slot to give).  Summaries: refresh_summaries."""
     B, H, Hq, NB, bs, D, S = _sizes(cfg)
     _check(k_new, (B, H, D), "k_new")
     _check(v_new, (B, H, D), "v_new")
@@ -212,11 +213,6 @@ def append_kv(cfg: dict, k_new, v_new, ctx_len, step, host_k, host_v, slot_of_bl
     _check(last_used, (B, H, S), "last_used")
     _check(pool_k, (B, H, S, bs, D), "pool_k")
     _check(pool_v, (B, H, S, bs, D), "pool_v")
-    _check(summ, (B, H, NB, D), "summ")
-    mm = None
-    if summ_mm is not None:
-        _check(summ_mm, (B, H, NB, 2, D), "summ_mm")
-        mm = _p(summ_mm, np.uint16)
     ck = None
     if clock is not None:
         _check(clock, (B, H), "clock")
@@ -225,7 +221,22 @@ def append_kv(cfg: dict, k_new, v_new, ctx_len, step, host_k, host_v, slot_of_bl
         C.byref(_cfg(cfg)), _p(k_new, np.uint16), _p(v_new, np.uint16), _p(ctx_len, np.int32), ck,
         int(step), _p(host_k, np.uint16), _p(host_v, np.uint16), _p(slot_of_block, np.int32),
         _p(block_of_slot, np.int32), _p(last_used, np.int32), _p(pool_k, np.uint16),
-        _p(pool_v, np.uint16), _p(summ, np.float32), mm))
+        _p(pool_v, np.uint16)))
+
+
+def refresh_summaries(cfg: dict, ctx_len, host_k, summ, summ_mm=None) -> None:
+    """Recomputes, in place, the summaries of each context's newest block over
+    its rows inside the context."""
+    B, H, Hq, NB, bs, D, S = _sizes(cfg)
+    _check(ctx_len, (B,), "ctx_len")
+    _check(host_k, (B, H, NB, bs, D), "host_k")
+    _check(summ, (B, H, NB, D), "summ")
+    mm = None
+    if summ_mm is not None:
+        _check(summ_mm, (B, H, NB, 2, D), "summ_mm")
+        mm = _p(summ_mm, np.uint16)
+    lib().orc_refresh_summaries(C.byref(_cfg(cfg)), _p(ctx_len, np.int32), _p(host_k, np.uint16),
+                                _p(summ, np.float32), mm)
 
 
 def plan_fetch(cfg: dict, topk_ids: np.ndarray, step: int, slot_of_block: np.ndarray,

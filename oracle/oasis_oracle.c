@@ -462,20 +462,17 @@ int orc_fetch_blocks(const orc_cfg* c, const uint16_t* host_k, const uint16_t* h
  *     window of n = j + 1 blocks, as in orc_select_topk_ctx), ties by lower
  *     block id -- with last_used = the step, and rows 0..t-1 of the block are
  *     copied in from the full cache.  Row t of the slot gets the token.
- *  3. The block's compressed keys cover its tokens in the context, rows
- *     0..t: the mean (summed in double in row order, divided by t+1, rounded
- *     once to fp32) and, if summ_mm is given, the max and min rows.
- *  4. ctx_len[b] = p + 1.
+ *  3. ctx_len[b] = p + 1.
+ * The block's compressed keys follow with orc_refresh_summaries.
  * The step is clock[b*H+h] when clock is given, else `step`.  A request whose
  * context is full (p >= NB*bs) or negative is left unchanged and the call
  * returns -1; a head with no slot to give (every resident block forced, none
- * empty) gets rows 1 and 3 only and the call returns -2.  Returns 0 otherwise.
+ * empty) gets row 1 only and the call returns -2.  Returns 0 otherwise.
  */
 int orc_append_kv(const orc_cfg* c, const uint16_t* k_new, const uint16_t* v_new,
                   int32_t* ctx_len, const int32_t* clock, int32_t step, uint16_t* host_k,
                   uint16_t* host_v, int32_t* slot_of_block, int32_t* block_of_slot,
-                  int32_t* last_used, uint16_t* pool_k, uint16_t* pool_v, float* summ,
-                  uint16_t* summ_mm)
+                  int32_t* last_used, uint16_t* pool_k, uint16_t* pool_v)
 {
     const int B = c->batch, H = c->num_kv_heads, NB = c->num_blocks;
     const int bs = c->block_size, D = c->head_dim, S = slots_of(c);
@@ -529,7 +526,37 @@ int orc_append_kv(const orc_cfg* c, const uint16_t* k_new, const uint16_t* v_new
                 memcpy(pool_k + ((u * S + s) * bs + t) * D, k_new + u * D, sizeof(uint16_t) * D);
                 memcpy(pool_v + ((u * S + s) * bs + t) * D, v_new + u * D, sizeof(uint16_t) * D);
             }
-            /* 3 */
+        }
+        /* 3 */
+        ctx_len[b] = p + 1;
+    }
+    return rc;
+}
+
+/*
+ * Compressed keys of each context's newest block after an append ([OasisKV]
+ * Fig. 7 left, over a growing context).  Reading: a block's summary covers
+ * its tokens inside the context.  For request b the last token is
+ * p = ctx_len[b] - 1 (nothing to do for an empty context); its block
+ * j = p / bs holds rows 0..t, t = p % bs, and for every KV head:
+ *   summ[b,h,j,:]  = the mean of those rows (summed in double in row order,
+ *                    divided by t + 1, rounded once to fp32);
+ *   summ_mm        (if given) their elementwise max and min, first row first
+ *                    on equal values, as orc_build_summaries_minmax.
+ * With a full block this is the summary orc_build_summaries gives.
+ */
+void orc_refresh_summaries(const orc_cfg* c, const int32_t* ctx_len, const uint16_t* host_k,
+                           float* summ, uint16_t* summ_mm)
+{
+    const int B = c->batch, H = c->num_kv_heads, NB = c->num_blocks;
+    const int bs = c->block_size, D = c->head_dim;
+    for (int b = 0; b < B; ++b) {
+        const long long p = (long long)ctx_len[b] - 1;
+        if (p < 0) continue;
+        const int j = (int)(p / bs), t = (int)(p % bs);
+        if (j >= NB) continue;
+        for (int h = 0; h < H; ++h) {
+            const size_t u = (size_t)b * H + h;
             for (int d = 0; d < D; ++d) {
                 const uint16_t* kb = host_k + (u * NB + j) * bs * D + d;
                 double sum = 0.0;
@@ -546,10 +573,7 @@ int orc_append_kv(const orc_cfg* c, const uint16_t* k_new, const uint16_t* v_new
                 }
             }
         }
-        /* 4 */
-        ctx_len[b] = p + 1;
     }
-    return rc;
 }
 
 /*

@@ -68,8 +68,9 @@ int  orc_select_topk_ctx(const orc_cfg* c, const float* scores, const int32_t* c
 int  orc_append_kv(const orc_cfg* c, const uint16_t* k_new, const uint16_t* v_new,
                    int32_t* ctx_len, const int32_t* clock, int32_t step, uint16_t* host_k,
                    uint16_t* host_v, int32_t* slot_of_block, int32_t* block_of_slot,
-                   int32_t* last_used, uint16_t* pool_k, uint16_t* pool_v, float* summ,
-                   uint16_t* summ_mm);
+                   int32_t* last_used, uint16_t* pool_k, uint16_t* pool_v);
+void orc_refresh_summaries(const orc_cfg* c, const int32_t* ctx_len, const uint16_t* host_k,
+                           float* summ, uint16_t* summ_mm);
 int  orc_plan_fetch(const orc_cfg* c, const int32_t* topk_ids, int32_t step,
                     int32_t* slot_of_block, int32_t* block_of_slot, int32_t* last_used,
                     int32_t* fetch_block, int32_t* fetch_slot, int32_t* evict_block,

@@ -22,6 +22,7 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "oasis.h")
 OASIS_OK, OASIS_ERR_INVALID_ARG, OASIS_ERR_UNSUPPORTED, OASIS_ERR_CUDA, OASIS_ERR_TIMEOUT = range(5)
 DEVERR_FETCH_RANGE, DEVERR_PLAN_STATE, DEVERR_TOPK_IDS, DEVERR_WAIT_TIMEOUT, DEVERR_SLOT_RANGE = (
     0x1, 0x2, 0x4, 0x8, 0x10)
+DEVERR_CTX_FULL, DEVERR_NO_SLOT = 0x20, 0x40
 
 
 class OasisError(RuntimeError):
@@ -70,6 +71,12 @@ _SIGS = {
                                                  C.c_float, _P, _P]),
     "oasis_build_summaries_minmax": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P]),
     "oasis_score_blocks_minmax": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P, _P]),
+    "oasis_select_topk_ctx": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P, _P]),
+    "oasis_predict_select_ctx": (C.c_int, [C.POINTER(OasisConfig), _P, _P, C.c_int32, _P, _P, _P,
+                                           _P, _P, _P, _P, _P, _P, _P, _P]),
+    "oasis_append_kv": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P, _P, C.c_int32, _P, _P, _P,
+                                  _P, _P, _P, _P, _P]),
+    "oasis_refresh_summaries": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P, _P, _P, _P, _P]),
     "oasis_host_register": (C.c_int, [_P, C.c_size_t, C.POINTER(C.c_void_p)]),
     "oasis_host_unregister": (C.c_int, [_P]),
     "oasis_device_errors": (C.c_int, [C.POINTER(C.c_uint32), C.c_int32]),
@@ -260,6 +267,73 @@ def oasis_predict_select(cfg, scores, step, clock, topk_ids, slot_of_block, bloc
         _ptr(fetch_block, i32, (B, H, w), "fetch_block"), _ptr(fetch_slot, i32, (B, H, w), "fetch_slot"),
         _ptr(evict_block, i32, (B, H, w), "evict_block"), _ptr(n_fetch, i32, (B, H), "n_fetch"),
         _ptr(n_evict, i32, (B, H), "n_evict"), _stream(stream)))
+
+
+def oasis_select_topk_ctx(cfg, scores, ctx_len, topk_ids, stream=None) -> None:
+    """Top-K with the local window at each request's context end (ctx_len [B])."""
+    c = OasisConfig.make(cfg)
+    B, H, Hq, NB, bs, D, S = _dims(c)
+    _check("oasis_select_topk_ctx", lib().oasis_select_topk_ctx(
+        C.byref(c), _ptr(scores, torch.float32, (B, H, NB), "scores"),
+        _ptr(ctx_len, torch.int32, (B,), "ctx_len"),
+        _ptr(topk_ids, torch.int32, (B, H, c.top_k), "topk_ids"), _stream(stream)))
+
+
+def oasis_predict_select_ctx(cfg, scores, ctx_len, step, clock, topk_ids, slot_of_block,
+                             block_of_slot, last_used, fetch_block, fetch_slot, evict_block,
+                             n_fetch, n_evict, stream=None) -> None:
+    """oasis_predict_select over a growing context (ctx_len [B])."""
+    c = OasisConfig.make(cfg)
+    B, H, Hq, NB, bs, D, S = _dims(c)
+    w = cap_width(c)
+    i32 = torch.int32
+    ck = C.c_void_p(0) if clock is None else _ptr(clock, i32, (B, H), "clock")
+    _check("oasis_predict_select_ctx", lib().oasis_predict_select_ctx(
+        C.byref(c), _ptr(scores, torch.float32, (B, H, NB), "scores"),
+        _ptr(ctx_len, i32, (B,), "ctx_len"), int(step), ck,
+        _ptr(topk_ids, i32, (B, H, c.top_k), "topk_ids"),
+        _ptr(slot_of_block, i32, (B, H, NB), "slot_of_block"),
+        _ptr(block_of_slot, i32, (B, H, S), "block_of_slot"),
+        _ptr(last_used, i32, (B, H, S), "last_used"),
+        _ptr(fetch_block, i32, (B, H, w), "fetch_block"), _ptr(fetch_slot, i32, (B, H, w), "fetch_slot"),
+        _ptr(evict_block, i32, (B, H, w), "evict_block"), _ptr(n_fetch, i32, (B, H), "n_fetch"),
+        _ptr(n_evict, i32, (B, H), "n_evict"), _stream(stream)))
+
+
+def oasis_append_kv(cfg, k_new, v_new, ctx_len, step, clock, host_k, host_v, slot_of_block,
+                    block_of_slot, last_used, pool_k, pool_v, stream=None) -> None:
+    """Appends one token per request (k_new, v_new [B, Hkv, D] bf16) at
+    ctx_len [B] and advances it.  host_k / host_v: device addresses of the
+    mapped pinned cache (ints) or device tensors."""
+    c = OasisConfig.make(cfg)
+    B, H, Hq, NB, bs, D, S = _dims(c)
+    i32, bf = torch.int32, torch.bfloat16
+    ck = C.c_void_p(0) if clock is None else _ptr(clock, i32, (B, H), "clock")
+    _check("oasis_append_kv", lib().oasis_append_kv(
+        C.byref(c), _ptr(k_new, bf, (B, H, D), "k_new"), _ptr(v_new, bf, (B, H, D), "v_new"),
+        _ptr(ctx_len, i32, (B,), "ctx_len"), ck, int(step),
+        _ptr(host_k, bf, (B, H, NB, bs, D), "host_k", device=False),
+        _ptr(host_v, bf, (B, H, NB, bs, D), "host_v", device=False),
+        _ptr(slot_of_block, i32, (B, H, NB), "slot_of_block"),
+        _ptr(block_of_slot, i32, (B, H, S), "block_of_slot"),
+        _ptr(last_used, i32, (B, H, S), "last_used"),
+        _ptr(pool_k, bf, (B, H, S, bs, D), "pool_k"), _ptr(pool_v, bf, (B, H, S, bs, D), "pool_v"),
+        _stream(stream)))
+
+
+def oasis_refresh_summaries(cfg, ctx_len, host_k, slot_of_block, pool_k, summ, summ_mm=None,
+                            stream=None) -> None:
+    """Summaries of each context's newest block over its rows in the context."""
+    c = OasisConfig.make(cfg)
+    B, H, Hq, NB, bs, D, S = _dims(c)
+    bf = torch.bfloat16
+    mm = C.c_void_p(0) if summ_mm is None else _ptr(summ_mm, bf, (B, H, NB, 2, D), "summ_mm")
+    _check("oasis_refresh_summaries", lib().oasis_refresh_summaries(
+        C.byref(c), _ptr(ctx_len, torch.int32, (B,), "ctx_len"),
+        _ptr(host_k, bf, (B, H, NB, bs, D), "host_k", device=False),
+        _ptr(slot_of_block, torch.int32, (B, H, NB), "slot_of_block"),
+        _ptr(pool_k, bf, (B, H, S, bs, D), "pool_k"),
+        _ptr(summ, torch.float32, (B, H, NB, D), "summ"), mm, _stream(stream)))
 
 
 def oasis_fetch_blocks(cfg, host_k, host_v, fetch_block, fetch_slot, n_fetch, pool_k, pool_v,

@@ -250,7 +250,21 @@ oasis_status_t oasis_select_topk(const oasis_config_t* cfg, const float* scores,
   if (!aligned(scores, 4) || !aligned(topk_ids, 4)) return OASIS_ERR_INVALID_ARG;
   DeviceInfo di;
   if ((st = device_info(&di)) != OASIS_OK) return st;
-  return from_cuda(launch_select_topk(s, scores, topk_ids, static_cast<cudaStream_t>(stream), di));
+  return from_cuda(
+      launch_select_topk(s, scores, nullptr, topk_ids, static_cast<cudaStream_t>(stream), di));
+}
+
+oasis_status_t oasis_select_topk_ctx(const oasis_config_t* cfg, const float* scores,
+                                     const int32_t* ctx_len, int32_t* topk_ids, void* stream) {
+  Shape s;
+  oasis_status_t st = make_shape(cfg, &s);
+  if (st != OASIS_OK) return st;
+  if (!aligned(scores, 4) || !aligned(topk_ids, 4) || !aligned(ctx_len, 4))
+    return OASIS_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != OASIS_OK) return st;
+  return from_cuda(
+      launch_select_topk(s, scores, ctx_len, topk_ids, static_cast<cudaStream_t>(stream), di));
 }
 
 oasis_status_t oasis_plan_fetch(const oasis_config_t* cfg, const int32_t* topk_ids, int32_t step,
@@ -308,10 +322,71 @@ oasis_status_t oasis_predict_select(const oasis_config_t* cfg, const float* scor
   if (clock && !aligned(clock, 4)) return OASIS_ERR_INVALID_ARG;
   DeviceInfo di;
   if ((st = device_info(&di)) != OASIS_OK) return st;
-  return from_cuda(launch_select_and_plan(s, scores, topk_ids, step, clock, slot_of_block,
+  return from_cuda(launch_select_and_plan(s, scores, nullptr, topk_ids, step, clock, slot_of_block,
                                           block_of_slot, last_used, fetch_block, fetch_slot,
                                           evict_block, n_fetch, n_evict,
                                           static_cast<cudaStream_t>(stream), di));
+}
+
+oasis_status_t oasis_predict_select_ctx(const oasis_config_t* cfg, const float* scores,
+                                        const int32_t* ctx_len, int32_t step, int32_t* clock,
+                                        int32_t* topk_ids, int32_t* slot_of_block,
+                                        int32_t* block_of_slot, int32_t* last_used,
+                                        int32_t* fetch_block, int32_t* fetch_slot,
+                                        int32_t* evict_block, int32_t* n_fetch, int32_t* n_evict,
+                                        void* stream) {
+  Shape s;
+  oasis_status_t st = make_shape(cfg, &s);
+  if (st != OASIS_OK) return st;
+  const void* ptrs[] = {scores, ctx_len, topk_ids, slot_of_block, block_of_slot, last_used,
+                        fetch_block, fetch_slot, evict_block, n_fetch, n_evict};
+  for (const void* p : ptrs)
+    if (!aligned(p, 4)) return OASIS_ERR_INVALID_ARG;
+  if (clock && !aligned(clock, 4)) return OASIS_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != OASIS_OK) return st;
+  return from_cuda(launch_select_and_plan(s, scores, ctx_len, topk_ids, step, clock, slot_of_block,
+                                          block_of_slot, last_used, fetch_block, fetch_slot,
+                                          evict_block, n_fetch, n_evict,
+                                          static_cast<cudaStream_t>(stream), di));
+}
+
+oasis_status_t oasis_append_kv(const oasis_config_t* cfg, const uint16_t* k_new,
+                               const uint16_t* v_new, int32_t* ctx_len, const int32_t* clock,
+                               int32_t step, uint16_t* host_k, uint16_t* host_v,
+                               int32_t* slot_of_block, int32_t* block_of_slot, int32_t* last_used,
+                               uint16_t* pool_k, uint16_t* pool_v, void* stream) {
+  Shape s;
+  oasis_status_t st = make_shape(cfg, &s);
+  if (st != OASIS_OK) return st;
+  if (s.Hkv > 32) return OASIS_ERR_UNSUPPORTED;
+  if (!aligned(k_new, 8) || !aligned(v_new, 8) || !aligned(host_k, 16) || !aligned(host_v, 16) ||
+      !aligned(pool_k, 16) || !aligned(pool_v, 16) || !aligned(ctx_len, 4) ||
+      !aligned(slot_of_block, 4) || !aligned(block_of_slot, 4) || !aligned(last_used, 4))
+    return OASIS_ERR_INVALID_ARG;
+  if (clock && !aligned(clock, 4)) return OASIS_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != OASIS_OK) return st;
+  return from_cuda(launch_append_kv(s, k_new, v_new, ctx_len, clock, step, host_k, host_v,
+                                    slot_of_block, block_of_slot, last_used, pool_k, pool_v,
+                                    static_cast<cudaStream_t>(stream), di));
+}
+
+oasis_status_t oasis_refresh_summaries(const oasis_config_t* cfg, const int32_t* ctx_len,
+                                       const uint16_t* host_k, const int32_t* slot_of_block,
+                                       const uint16_t* pool_k, float* summ, uint16_t* summ_mm,
+                                       void* stream) {
+  Shape s;
+  oasis_status_t st = make_shape(cfg, &s);
+  if (st != OASIS_OK) return st;
+  if (!aligned(ctx_len, 4) || !aligned(host_k, 16) || !aligned(slot_of_block, 4) ||
+      !aligned(pool_k, 16) || !aligned(summ, 16))
+    return OASIS_ERR_INVALID_ARG;
+  if (summ_mm && !aligned(summ_mm, 16)) return OASIS_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != OASIS_OK) return st;
+  return from_cuda(launch_refresh_summaries(s, ctx_len, host_k, slot_of_block, pool_k, summ,
+                                            summ_mm, static_cast<cudaStream_t>(stream), di));
 }
 
 oasis_status_t oasis_fetch_blocks(const oasis_config_t* cfg, const uint16_t* host_k,

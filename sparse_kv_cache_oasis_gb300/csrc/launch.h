@@ -35,14 +35,15 @@ cudaError_t launch_build_summaries_minmax(const Shape& s, const uint16_t* k, uin
 cudaError_t launch_score_blocks_minmax(const Shape& s, const uint16_t* q_draft,
                                        const uint16_t* summ_mm, float* scores, cudaStream_t st,
                                        const DeviceInfo& di);
-cudaError_t launch_select_topk(const Shape& s, const float* scores, int32_t* topk_ids,
-                               cudaStream_t st, const DeviceInfo& di);
+cudaError_t launch_select_topk(const Shape& s, const float* scores, const int32_t* ctx_len,
+                               int32_t* topk_ids, cudaStream_t st, const DeviceInfo& di);
 cudaError_t launch_plan_fetch(const Shape& s, const int32_t* topk_ids, int32_t step,
                               int32_t* clock, int32_t* slot_of_block, int32_t* block_of_slot,
                               int32_t* last_used, int32_t* fetch_block, int32_t* fetch_slot,
                               int32_t* evict_block, int32_t* n_fetch, int32_t* n_evict,
                               cudaStream_t st, const DeviceInfo& di);
-cudaError_t launch_select_and_plan(const Shape& s, const float* scores, int32_t* topk_ids,
+cudaError_t launch_select_and_plan(const Shape& s, const float* scores, const int32_t* ctx_len,
+                                   int32_t* topk_ids,
                                    int32_t step, int32_t* clock, int32_t* slot_of_block,
                                    int32_t* block_of_slot, int32_t* last_used,
                                    int32_t* fetch_block, int32_t* fetch_slot,
@@ -52,6 +53,17 @@ cudaError_t launch_fetch_blocks(const Shape& s, const uint16_t* host_k, const ui
                                 const int32_t* fetch_block, const int32_t* fetch_slot,
                                 const int32_t* n_fetch, uint16_t* pool_k, uint16_t* pool_v,
                                 cudaStream_t st, const DeviceInfo& di);
+
+// Decode-time append of one token per request (write-allocate of the newest block).
+cudaError_t launch_append_kv(const Shape& s, const uint16_t* k_new, const uint16_t* v_new,
+                             int32_t* ctx_len, const int32_t* clock, int32_t step,
+                             uint16_t* host_k, uint16_t* host_v, int32_t* slot_of_block,
+                             int32_t* block_of_slot, int32_t* last_used, uint16_t* pool_k,
+                             uint16_t* pool_v, cudaStream_t st, const DeviceInfo& di);
+cudaError_t launch_refresh_summaries(const Shape& s, const int32_t* ctx_len,
+                                     const uint16_t* host_k, const int32_t* slot_of_block,
+                                     const uint16_t* pool_k, float* summ, uint16_t* summ_mm,
+                                     cudaStream_t st, const DeviceInfo& di);
 
 // Attention: the pools are read by TMA through these two tensor maps.
 size_t attn_workspace_bytes(const Shape& s);

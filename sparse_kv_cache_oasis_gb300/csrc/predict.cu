@@ -104,17 +104,31 @@ struct PredLayout {
   }
 };
 
+// Blocks in the context of request b: ceil(ctx_len[b] / bs), at most NB
+// (all NB without a context length).
+__device__ __forceinline__ int context_blocks(const int32_t* ctx_len, int b, int bs, int NB) {
+  if (!ctx_len) return NB;
+  const int c = ctx_len[b];
+  if (c <= 0) return 0;
+  const long long n = (static_cast<long long>(c) + bs - 1) / bs;
+  return n < NB ? static_cast<int>(n) : NB;
+}
+
 // Writes the unit's top-K list (priority order) to `out_smem` (K ints) and,
 // if out_global is not null, to global memory.  All threads must call it.
-template <int ITEMS>
-__device__ void topk_unit(const float* __restrict__ sc, int NB, int K, int sink, int local,
-                          int* out_smem, int32_t* __restrict__ out_global, const TopkSmem& sm) {
+// `nblk` blocks are in the context: the local window ends there, and blocks at
+// or beyond it rank as if scored -infinity (nblk = NB: the whole cache).
+template <int ITEMS, bool CTX>
+__device__ void topk_unit(const float* __restrict__ sc, int NB, int nblk_arg, int K, int sink,
+                          int local, int* out_smem, int32_t* __restrict__ out_global,
+                          const TopkSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T = blockDim.x;
-  const int a = sink < NB ? sink : NB;
-  const int b0 = NB - local > 0 ? NB - local : 0;
+  const int nblk = CTX ? nblk_arg : NB;  // without a context length: the whole cache
+  const int a = sink < nblk ? sink : nblk;
+  const int b0 = nblk - local > 0 ? nblk - local : 0;
   const int lo = a > b0 ? a : b0;
-  const int F = a + (NB - lo);
+  const int F = a + (nblk - lo);
   const int need = K - F;
   for (int i = tid; i < F && i < K; i += T) {
     const int id = i < a ? i : lo + (i - a);
@@ -130,8 +144,13 @@ __device__ void topk_unit(const float* __restrict__ sc, int NB, int K, int sink,
 #pragma unroll
   for (int it = 0; it < ITEMS; ++it) {
     const int j = tid + it * T;
-    valid[it] = j < NB && !(j < a || j >= lo);
-    key[it] = valid[it] ? orderable(__ldcg(sc + j)) : 0u;
+    if constexpr (CTX) {
+      valid[it] = j < NB && !(j < a || (j >= lo && j < nblk));
+      key[it] = valid[it] ? orderable(j < nblk ? __ldcg(sc + j) : -INFINITY) : 0u;
+    } else {
+      valid[it] = j < NB && !(j < a || j >= lo);
+      key[it] = valid[it] ? orderable(__ldcg(sc + j)) : 0u;
+    }
   }
   uint32_t prefix = 0u, mask = 0u;
   int remaining = need;
@@ -384,18 +403,20 @@ __device__ void plan_unit(const int* P, const SlotView v, int32_t step, int32_t*
 }
 
 // ---------------------------------------------------------------- kernels
-template <int ITEMS>
+template <int ITEMS, bool CTX>
 __global__ void __launch_bounds__(kPredThreads) topk_kernel(const float* __restrict__ scores,
+                                                            const int32_t* __restrict__ ctx_len,
                                                             int32_t* __restrict__ topk_ids,
                                                             int NB, int K, int sink, int local,
-                                                            PredLayout lay) {
+                                                            int Hkv, int bs, PredLayout lay) {
   extern __shared__ __align__(16) unsigned char pred_smem[];
   int* sP;
   TopkSmem tk;
   PlanSmem pl;
   lay.carve(pred_smem, &sP, &tk, &pl);
   const int64_t u = blockIdx.x;
-  topk_unit<ITEMS>(scores + u * NB, NB, K, sink, local, sP, topk_ids + u * K, tk);
+  const int nblk = CTX ? context_blocks(ctx_len, static_cast<int>(u / Hkv), bs, NB) : NB;
+  topk_unit<ITEMS, CTX>(scores + u * NB, NB, nblk, K, sink, local, sP, topk_ids + u * K, tk);
 }
 
 __global__ void __launch_bounds__(kPredThreads) plan_kernel(
@@ -422,15 +443,16 @@ __global__ void __launch_bounds__(kPredThreads) plan_kernel(
 }
 
 // Top-K and plan of one unit in one CTA; the map loads overlap the selection.
-template <int ITEMS>
+template <int ITEMS, bool CTX>
 __global__ void __launch_bounds__(kPredThreads) topk_plan_kernel(
-    const float* __restrict__ scores, int32_t* __restrict__ topk_ids, int32_t step,
+    const float* __restrict__ scores, const int32_t* __restrict__ ctx_len,
+    int32_t* __restrict__ topk_ids, int32_t step,
     int32_t* __restrict__ clock, int32_t* __restrict__ slot_of_block,
     int32_t* __restrict__ block_of_slot, int32_t* __restrict__ last_used,
     int32_t* __restrict__ fetch_block, int32_t* __restrict__ fetch_slot,
     int32_t* __restrict__ evict_block, int32_t* __restrict__ n_fetch,
     int32_t* __restrict__ n_evict, int NB, int S, int K, int cap, int capw, int sink, int local,
-    uint32_t* err, PredLayout lay) {
+    int Hkv, int bs, uint32_t* err, PredLayout lay) {
   extern __shared__ __align__(16) unsigned char pred_smem[];
   int* sP;
   TopkSmem tk;
@@ -440,7 +462,8 @@ __global__ void __launch_bounds__(kPredThreads) topk_plan_kernel(
   const int32_t st = clock ? clock[u] : step;
   int32_t* sob = slot_of_block + u * NB;
   const SlotView v = load_slot_view(sob, block_of_slot + u * S, last_used + u * S, S, NB);
-  topk_unit<ITEMS>(scores + u * NB, NB, K, sink, local, sP, topk_ids + u * K, tk);
+  const int nblk = CTX ? context_blocks(ctx_len, static_cast<int>(u / Hkv), bs, NB) : NB;
+  topk_unit<ITEMS, CTX>(scores + u * NB, NB, nblk, K, sink, local, sP, topk_ids + u * K, tk);
   plan_unit(sP, v, st, clock ? clock + u : nullptr, sob, block_of_slot + u * S, last_used + u * S,
             fetch_block + u * capw, fetch_slot + u * capw, evict_block + u * capw, n_fetch + u,
             n_evict + u, NB, S, K, cap, capw, err, pl);
@@ -468,9 +491,13 @@ static PredLayout pred_layout(const Shape& s) {
 template <int N>
 static cudaError_t pred_configure_n() {
   const int c = cudaSharedmemCarveoutMaxShared;
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel<N>, cudaFuncAttributePreferredSharedMemoryCarveout, c);
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel<N, false>, cudaFuncAttributePreferredSharedMemoryCarveout, c);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(topk_plan_kernel<N>, cudaFuncAttributePreferredSharedMemoryCarveout, c);
+    e = cudaFuncSetAttribute(topk_kernel<N, true>, cudaFuncAttributePreferredSharedMemoryCarveout, c);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(topk_plan_kernel<N, false>, cudaFuncAttributePreferredSharedMemoryCarveout, c);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(topk_plan_kernel<N, true>, cudaFuncAttributePreferredSharedMemoryCarveout, c);
   return e;
 }
 
@@ -497,15 +524,19 @@ cudaError_t pred_configure() {
     return cudaErrorInvalidValue;       \
   } while (0)
 
-cudaError_t launch_select_topk(const Shape& s, const float* scores, int32_t* topk_ids,
-                               cudaStream_t st, const DeviceInfo&) {
+cudaError_t launch_select_topk(const Shape& s, const float* scores, const int32_t* ctx_len,
+                               int32_t* topk_ids, cudaStream_t st, const DeviceInfo&) {
   const int T = pred_threads(s.K, s.NB);
   const int items = (s.NB + T - 1) / T;
   const PredLayout lay = pred_layout(s);
 #define OASIS_TOPK(N)                                                                              \
   {                                                                                                \
-    topk_kernel<N><<<s.units(), T, lay.bytes(), st>>>(scores, topk_ids, s.NB, s.K, s.sink, s.local, \
-                                                      lay);                                        \
+    if (ctx_len)                                                                                   \
+      topk_kernel<N, true><<<s.units(), T, lay.bytes(), st>>>(scores, ctx_len, topk_ids, s.NB, s.K,   \
+                                                              s.sink, s.local, s.Hkv, s.bs, lay);   \
+    else                                                                                           \
+      topk_kernel<N, false><<<s.units(), T, lay.bytes(), st>>>(scores, ctx_len, topk_ids, s.NB, s.K,  \
+                                                               s.sink, s.local, s.Hkv, s.bs, lay);  \
     return cudaGetLastError();                                                                     \
   }
   OASIS_ITEMS_SWITCH(items, OASIS_TOPK);
@@ -526,7 +557,8 @@ cudaError_t launch_plan_fetch(const Shape& s, const int32_t* topk_ids, int32_t s
   return cudaGetLastError();
 }
 
-cudaError_t launch_select_and_plan(const Shape& s, const float* scores, int32_t* topk_ids,
+cudaError_t launch_select_and_plan(const Shape& s, const float* scores, const int32_t* ctx_len,
+                                   int32_t* topk_ids,
                                    int32_t step, int32_t* clock, int32_t* slot_of_block,
                                    int32_t* block_of_slot, int32_t* last_used,
                                    int32_t* fetch_block, int32_t* fetch_slot,
@@ -539,10 +571,16 @@ cudaError_t launch_select_and_plan(const Shape& s, const float* scores, int32_t*
   const PredLayout lay = pred_layout(s);
 #define OASIS_TP(N)                                                                             \
   {                                                                                             \
-    topk_plan_kernel<N><<<s.units(), T, lay.bytes(), st>>>(                                     \
-        scores, topk_ids, step, clock, slot_of_block, block_of_slot, last_used, fetch_block,    \
-        fetch_slot, evict_block, n_fetch, n_evict, s.NB, s.S, s.K, s.cap, capw, s.sink,         \
-        s.local, di.err, lay);                                                                  \
+    if (ctx_len)                                                                                \
+      topk_plan_kernel<N, true><<<s.units(), T, lay.bytes(), st>>>(                             \
+          scores, ctx_len, topk_ids, step, clock, slot_of_block, block_of_slot, last_used,      \
+          fetch_block, fetch_slot, evict_block, n_fetch, n_evict, s.NB, s.S, s.K, s.cap, capw,   \
+          s.sink, s.local, s.Hkv, s.bs, di.err, lay);                                           \
+    else                                                                                        \
+      topk_plan_kernel<N, false><<<s.units(), T, lay.bytes(), st>>>(                            \
+          scores, ctx_len, topk_ids, step, clock, slot_of_block, block_of_slot, last_used,      \
+          fetch_block, fetch_slot, evict_block, n_fetch, n_evict, s.NB, s.S, s.K, s.cap, capw,   \
+          s.sink, s.local, s.Hkv, s.bs, di.err, lay);                                           \
     return cudaGetLastError();                                                                  \
   }
   OASIS_ITEMS_SWITCH(items, OASIS_TP);

@@ -132,6 +132,27 @@ class LayerState:
         """Scoring against the min/max compressed keys into self.scores."""
         ob.oasis_score_blocks_minmax(self.cfg, q_draft, self.summ_mm, self.scores, stream)
 
+    def append(self, k_new, v_new, stream=None):
+        """Decode-time append of one token per request at self.ctx_len (which
+        it advances): cache and working set (newest block kept resident, LRU
+        time from the device clock).  refresh_summaries follows."""
+        ob.oasis_append_kv(self.cfg, k_new, v_new, self.ctx_len, 0, self.clock, self.host_k_dev,
+                           self.host_v_dev, self.slot_of_block, self.block_of_slot, self.last_used,
+                           self.pool_k, self.pool_v, stream)
+
+    def refresh_summaries(self, stream=None):
+        """The newest block's summaries (min/max too when built) after an append."""
+        ob.oasis_refresh_summaries(self.cfg, self.ctx_len, self.host_k_dev, self.slot_of_block,
+                                   self.pool_k, self.summ, getattr(self, "summ_mm", None), stream)
+
+    def select_ctx(self, stream=None):
+        """Top-K with the local window at each context's end, then the plan,
+        in one launch (device clock)."""
+        ob.oasis_predict_select_ctx(self.cfg, self.scores, self.ctx_len, 0, self.clock, self.topk,
+                                    self.slot_of_block, self.block_of_slot, self.last_used,
+                                    self.fetch_block, self.fetch_slot, self.evict_block,
+                                    self.n_fetch, self.n_evict, stream)
+
     def predict_clocked(self, q_draft, stream=None):
         """predict() with the step taken from (and advanced in) self.clock."""
         ob.oasis_score_blocks(self.cfg, q_draft, self.summ, self.scores, stream)

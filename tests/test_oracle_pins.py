@@ -577,8 +577,10 @@ def test_append_writes_token_summary_and_working_set():
     cfg, hk, hv, kn, vn, sob, bos, lu, pk, pv, summ, mm = _append_setup()
     hk0, pk0, pv0 = hk.copy(), pk.copy(), pv.copy()
     ctx = np.asarray([32, 40], np.int32)       # request 0 starts block 2; request 1 is at row 8 of it
-    rc = oracle.append_kv(cfg, kn, vn, ctx, 9, hk, hv, sob, bos, lu, pk, pv, summ, mm)
+    rc = oracle.append_kv(cfg, kn, vn, ctx, 9, hk, hv, sob, bos, lu, pk, pv)
     assert rc == 0 and ctx.tolist() == [33, 41]
+    summ0 = summ.copy()
+    oracle.refresh_summaries(cfg, ctx, hk, summ, mm)
     for b, t in ((0, 0), (1, 8)):
         for h in range(2):
             assert np.array_equal(hk[b, h, 2, t], kn[b, h]) and np.array_equal(hv[b, h, 2, t], vn[b, h])
@@ -601,6 +603,20 @@ def test_append_writes_token_summary_and_working_set():
     assert np.array_equal(pk[1, 1, 2, 9:], pk0[1, 1, 2, 9:])      # rows past the context untouched
     # blocks other than 2 keep their summaries and cache rows
     assert np.array_equal(np.delete(hk, 2, axis=2), np.delete(hk0, 2, axis=2))
+    assert np.array_equal(np.delete(summ, 2, axis=2), np.delete(summ0, 2, axis=2))
+
+
+def test_refresh_of_a_full_block_is_the_build():
+    cfg, hk, hv, kn, vn, sob, bos, lu, pk, pv, summ, mm = _append_setup()
+    full = np.asarray([16 * 6, 16 * 3], np.int32)  # last blocks 5 and 2, both complete
+    oracle.refresh_summaries(cfg, full, hk, summ, mm)
+    ref, ref_mm = oracle.build_summaries(cfg, hk), oracle.build_summaries_minmax(cfg, hk)
+    assert np.array_equal(summ[0, :, 5], ref[0, :, 5]) and np.array_equal(summ[1, :, 2], ref[1, :, 2])
+    assert np.array_equal(mm[0, :, 5], ref_mm[0, :, 5]) and np.array_equal(mm[1, :, 2], ref_mm[1, :, 2])
+    # an empty context changes nothing
+    before = summ.copy()
+    oracle.refresh_summaries(cfg, np.asarray([0, 0], np.int32), hk, summ, mm)
+    assert np.array_equal(summ, before)
 
 
 def test_append_full_context_and_no_free_slot():
@@ -612,8 +628,9 @@ def test_append_full_context_and_no_free_slot():
     sob[1, 1] = -1
     sob[1, 1, 0], sob[1, 1, 2], sob[1, 1, 3] = 0, 1, 2
     hk0, pk0, bos0, sob0 = hk.copy(), pk.copy(), bos.copy(), sob.copy()
-    rc = oracle.append_kv(full, kn, vn, ctx, 3, hk, hv, sob, bos, lu, pk, pv, summ, mm)
+    rc = oracle.append_kv(full, kn, vn, ctx, 3, hk, hv, sob, bos, lu, pk, pv)
     assert rc == -1 and ctx.tolist() == [96, 65]
+    oracle.refresh_summaries(full, ctx, hk, summ, mm)
     assert np.array_equal(hk[0], hk0[0]) and np.array_equal(pk[0], pk0[0])   # request 0 untouched
     # (1,1): blocks 0 (sink), 2 and 3 (window of block 4) are forced: no slot, pool untouched
     assert np.array_equal(bos[1, 1], bos0[1, 1]) and np.array_equal(pk[1, 1], pk0[1, 1])
@@ -621,8 +638,7 @@ def test_append_full_context_and_no_free_slot():
     assert np.array_equal(summ[1, 1, 4], f32(kn[1, 1]))
     # (1,0): block 4 resident in slot 2 -> row 0 written there
     assert np.array_equal(pk[1, 0, 2, 0], kn[1, 0])
-    rc = oracle.append_kv(full, kn, vn, np.asarray([5, 70], np.int32), 3, hk, hv, sob, bos, lu, pk, pv,
-                          summ, mm)
+    rc = oracle.append_kv(full, kn, vn, np.asarray([5, 70], np.int32), 3, hk, hv, sob, bos, lu, pk, pv)
     assert rc == -2
 
 
