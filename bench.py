@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-grow", action="store_true", help="skip the growing-context run")
+    ap.add_argument("--profile-chain", type=int, default=0,
+                    help="with --profile-steps: then this many prediction-chain launches")
     ap.add_argument("--profile-grow", action="store_true",
                     help="with --profile-steps: run the growing-context form of the step")
     ap.add_argument("--profile-steps", type=int, default=0,
@@ -123,7 +125,8 @@ def algorithmic_bytes(wl, n_fetch_blocks: float, valid_slots: float):
     joint = valid_slots * blk + 2 * rows_io + U * wl.slots * 4
     return dict(attn=attn, score=score, fused=attn + score, topk=topk, plan=plan, fetch=fetch_hbm,
                 hbm=attn + score + topk + plan + fetch_hbm, link=link, joint=joint,
-                score_mm=score)  # bf16 max + min rows: as many bytes as the fp32 mean
+                score_mm=score,  # bf16 max + min rows: as many bytes as the fp32 mean
+                chain=score + topk + plan, score_select=score + topk + plan)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -614,9 +617,12 @@ def gpu_arm(args):
                 L.build_minmax_summaries()
         for r in range(args.profile_minmax):  # then min/max scoring launches
             layers[r % n_inst].score_minmax(qd_dev[r % n_inst][0], compute)
+        for r in range(args.profile_chain):  # then prediction-chain launches
+            layers[r % n_inst].predict_chain(qd_dev[r % n_inst][0], compute)
         torch.cuda.synchronize()
         print(json.dumps({"profile_steps": args.profile_steps, "profile_joint": args.profile_joint,
-                          "profile_minmax": args.profile_minmax}), flush=True)
+                          "profile_minmax": args.profile_minmax, "profile_chain": args.profile_chain}),
+              flush=True)
         return
 
     # ---- warm-up and timed region
@@ -672,12 +678,20 @@ def gpu_arm(args):
                     L.attention_joint(q_dev[i][0], qd_dev[i][0], compute)
                 elif kind == "score_mm":
                     L.score_minmax(qd_dev[i][0], compute)
+                elif kind == "chain":
+                    L.predict_chain(qd_dev[i][0], compute)
+                elif kind == "score_select":  # the same chain as two launches
+                    ob.oasis_score_blocks(L.cfg, qd_dev[i][0], L.summ, L.scores, compute)
+                    ob.oasis_predict_select(
+                        L.cfg, L.scores, 0, L.clock, L.topk, L.slot_of_block, L.block_of_slot,
+                        L.last_used, L.fetch_block, L.fetch_slot, L.evict_block, L.n_fetch,
+                        L.n_evict, compute)
         return g
 
     for L in layers:  # min/max compressed keys for the scoring variant (set-up)
         L.build_minmax_summaries()
     torch.cuda.synchronize()
-    kinds = ["attn", "score", "topk", "fused", "joint", "score_mm"]
+    kinds = ["attn", "score", "topk", "fused", "joint", "score_mm", "chain", "score_select"]
     mean_ms = {}
     for kind in kinds:
         g = kernel_graph(kind)
@@ -863,6 +877,13 @@ def gpu_arm(args):
                 "achieved_gbs": by["score_mm"] / (mean_ms["score_mm"] * 1e-3) / 1e9,
                 "frac_of_measured_hbm": by["score_mm"] / (mean_ms["score_mm"] * 1e-3) / 1e9 / peak,
                 "vs_mean_scoring": mean_ms["score_mm"] / mean_ms["score"]},
+            "predict_chain": {
+                "kernel": "chain_kernel", "ms_per_launch": mean_ms["chain"],
+                "bytes_per_launch": by["chain"],
+                "achieved_gbs": by["chain"] / (mean_ms["chain"] * 1e-3) / 1e9,
+                "frac_of_measured_hbm": by["chain"] / (mean_ms["chain"] * 1e-3) / 1e9 / peak,
+                "separate_launches_ms": mean_ms["score_select"],
+                "vs_separate_launches": mean_ms["chain"] / mean_ms["score_select"]},
             "growing_context": grow,
             "kernels_ms": mean_ms,
             "kernel_gbs": {k: by[k] / (mean_ms[k] * 1e-3) / 1e9 for k in kinds},

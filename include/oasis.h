@@ -15,6 +15,7 @@
  *   oasis_score_blocks         draft queries scan compressed keys  (Fig. 7 right)
  *   oasis_score_blocks_minmax  the same against min/max-pooled keys (Fig. 7 left)
  *   oasis_select_topk          top-K blocks per KV head            (diagram step 2)
+ *   oasis_predict_chain        scoring + top-K + plan in one launch (diagram steps 2-3)
  *   oasis_plan_fetch           diff vs. working set, capped LRU    (diagram step 3, Tab. 2)
  *   oasis_fetch_blocks         host -> HBM transfer, copy stream   (diagram step 4, Fig. 8)
  *   oasis_append_kv            the decoded token joins cache and working set (Fig. 8)
@@ -217,6 +218,20 @@ oasis_status_t oasis_predict_select(const oasis_config_t* cfg, const float* scor
                                     int32_t* last_used, int32_t* fetch_block,
                                     int32_t* fetch_slot, int32_t* evict_block,
                                     int32_t* n_fetch, int32_t* n_evict, void* stream);
+
+/* The whole prediction chain in one launch ([OasisKV] Fig. 7 right, diagram
+ * steps 2-3): oasis_score_blocks(cfg, q_draft, summ, scores) followed by
+ * oasis_predict_select(cfg, scores, step, clock, ...), with the same results
+ * bit for bit (scores are written too).  The CTAs scoring one (request, KV
+ * head) form a thread-block cluster; after a cluster barrier the unit's first
+ * CTA selects and plans.  Supported: L*G <= 32, S <= 256, K <= 256,
+ * NB <= 8192 (else OASIS_ERR_UNSUPPORTED).  Alignment as for the two calls. */
+oasis_status_t oasis_predict_chain(const oasis_config_t* cfg, const uint16_t* q_draft,
+                                   const float* summ, float* scores, int32_t step, int32_t* clock,
+                                   int32_t* topk_ids, int32_t* slot_of_block,
+                                   int32_t* block_of_slot, int32_t* last_used,
+                                   int32_t* fetch_block, int32_t* fetch_slot, int32_t* evict_block,
+                                   int32_t* n_fetch, int32_t* n_evict, void* stream);
 
 /* oasis_predict_select with the top-K of oasis_select_topk_ctx (the window
  * follows each request's context length ctx_len [B]). */

@@ -77,6 +77,8 @@ _SIGS = {
     "oasis_append_kv": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P, _P, C.c_int32, _P, _P, _P,
                                   _P, _P, _P, _P, _P]),
     "oasis_refresh_summaries": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P, _P, _P, _P, _P]),
+    "oasis_predict_chain": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P, C.c_int32, _P, _P, _P,
+                                      _P, _P, _P, _P, _P, _P, _P, _P]),
     "oasis_host_register": (C.c_int, [_P, C.c_size_t, C.POINTER(C.c_void_p)]),
     "oasis_host_unregister": (C.c_int, [_P]),
     "oasis_device_errors": (C.c_int, [C.POINTER(C.c_uint32), C.c_int32]),
@@ -260,6 +262,28 @@ def oasis_predict_select(cfg, scores, step, clock, topk_ids, slot_of_block, bloc
     ck = C.c_void_p(0) if clock is None else _ptr(clock, i32, (B, H), "clock")
     _check("oasis_predict_select", lib().oasis_predict_select(
         C.byref(c), _ptr(scores, torch.float32, (B, H, NB), "scores"), int(step), ck,
+        _ptr(topk_ids, i32, (B, H, c.top_k), "topk_ids"),
+        _ptr(slot_of_block, i32, (B, H, NB), "slot_of_block"),
+        _ptr(block_of_slot, i32, (B, H, S), "block_of_slot"),
+        _ptr(last_used, i32, (B, H, S), "last_used"),
+        _ptr(fetch_block, i32, (B, H, w), "fetch_block"), _ptr(fetch_slot, i32, (B, H, w), "fetch_slot"),
+        _ptr(evict_block, i32, (B, H, w), "evict_block"), _ptr(n_fetch, i32, (B, H), "n_fetch"),
+        _ptr(n_evict, i32, (B, H), "n_evict"), _stream(stream)))
+
+
+def oasis_predict_chain(cfg, q_draft, summ, scores, step, clock, topk_ids, slot_of_block,
+                        block_of_slot, last_used, fetch_block, fetch_slot, evict_block, n_fetch,
+                        n_evict, stream=None) -> None:
+    """Scoring, top-K and plan in one launch; `clock` ([B, Hkv] int32) or None."""
+    c = OasisConfig.make(cfg)
+    B, H, Hq, NB, bs, D, S = _dims(c)
+    w = cap_width(c)
+    i32 = torch.int32
+    ck = C.c_void_p(0) if clock is None else _ptr(clock, i32, (B, H), "clock")
+    _check("oasis_predict_chain", lib().oasis_predict_chain(
+        C.byref(c), _ptr(q_draft, torch.bfloat16, (B, c.lookahead, Hq, D), "q_draft"),
+        _ptr(summ, torch.float32, (B, H, NB, D), "summ"),
+        _ptr(scores, torch.float32, (B, H, NB), "scores"), int(step), ck,
         _ptr(topk_ids, i32, (B, H, c.top_k), "topk_ids"),
         _ptr(slot_of_block, i32, (B, H, NB), "slot_of_block"),
         _ptr(block_of_slot, i32, (B, H, S), "block_of_slot"),

@@ -50,6 +50,7 @@ oasis_status_t device_info(DeviceInfo* out) {
     if (fetch_configure() != cudaSuccess) return OASIS_ERR_CUDA;
     if (fused_configure() != cudaSuccess) return OASIS_ERR_CUDA;
     if (joint_configure() != cudaSuccess) return OASIS_ERR_CUDA;
+    if (chain_configure() != cudaSuccess) return OASIS_ERR_CUDA;
     di.score_ctas_per_sm = score_ctas_per_sm();
     di.attn_ctas_per_sm = attn_ctas_per_sm();
     d.info = di;
@@ -326,6 +327,31 @@ oasis_status_t oasis_predict_select(const oasis_config_t* cfg, const float* scor
                                           block_of_slot, last_used, fetch_block, fetch_slot,
                                           evict_block, n_fetch, n_evict,
                                           static_cast<cudaStream_t>(stream), di));
+}
+
+oasis_status_t oasis_predict_chain(const oasis_config_t* cfg, const uint16_t* q_draft,
+                                   const float* summ, float* scores, int32_t step, int32_t* clock,
+                                   int32_t* topk_ids, int32_t* slot_of_block,
+                                   int32_t* block_of_slot, int32_t* last_used,
+                                   int32_t* fetch_block, int32_t* fetch_slot, int32_t* evict_block,
+                                   int32_t* n_fetch, int32_t* n_evict, void* stream) {
+  Shape s;
+  oasis_status_t st = make_shape(cfg, &s);
+  if (st != OASIS_OK) return st;
+  if (!chain_supported(s)) return OASIS_ERR_UNSUPPORTED;
+  if (!aligned(q_draft, 16) || !aligned(summ, 16) || !aligned(scores, 8))
+    return OASIS_ERR_INVALID_ARG;
+  const void* ptrs[] = {topk_ids, slot_of_block, block_of_slot, last_used,
+                        fetch_block, fetch_slot, evict_block, n_fetch, n_evict};
+  for (const void* p : ptrs)
+    if (!aligned(p, 4)) return OASIS_ERR_INVALID_ARG;
+  if (clock && !aligned(clock, 4)) return OASIS_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != OASIS_OK) return st;
+  return from_cuda(launch_predict_chain(s, q_draft, summ, scores, step, clock, topk_ids,
+                                        slot_of_block, block_of_slot, last_used, fetch_block,
+                                        fetch_slot, evict_block, n_fetch, n_evict,
+                                        static_cast<cudaStream_t>(stream), di));
 }
 
 oasis_status_t oasis_predict_select_ctx(const oasis_config_t* cfg, const float* scores,

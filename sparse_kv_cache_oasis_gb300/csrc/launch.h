@@ -78,6 +78,16 @@ cudaError_t launch_sparse_decode_attn(const Shape& s, const uint16_t* q,
                                       cudaStream_t st, const DeviceInfo& di);
 int attn_split(const Shape& s, int sm_count);  // CTAs per unit (cluster size)
 
+// Scoring, top-K and plan of every unit in one launch (clusters per unit).
+bool chain_supported(const Shape& s);
+cudaError_t chain_configure();  // one-time function attributes
+cudaError_t launch_predict_chain(const Shape& s, const uint16_t* q_draft, const float* summ,
+                                 float* scores, int32_t step, int32_t* clock, int32_t* topk_ids,
+                                 int32_t* slot_of_block, int32_t* block_of_slot,
+                                 int32_t* last_used, int32_t* fetch_block, int32_t* fetch_slot,
+                                 int32_t* evict_block, int32_t* n_fetch, int32_t* n_evict,
+                                 cudaStream_t st, const DeviceInfo& di);
+
 // Joint attention of the decoded and the draft tokens: row tiles per CTA,
 // row groups per unit and CTAs per (unit, row group).
 struct JointSplit {

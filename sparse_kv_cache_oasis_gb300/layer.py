@@ -153,6 +153,13 @@ class LayerState:
                                     self.fetch_block, self.fetch_slot, self.evict_block,
                                     self.n_fetch, self.n_evict, stream)
 
+    def predict_chain(self, q_draft, stream=None):
+        """Scoring, top-K and planning in one launch (device clock)."""
+        ob.oasis_predict_chain(self.cfg, q_draft, self.summ, self.scores, 0, self.clock,
+                               self.topk, self.slot_of_block, self.block_of_slot, self.last_used,
+                               self.fetch_block, self.fetch_slot, self.evict_block, self.n_fetch,
+                               self.n_evict, stream)
+
     def predict_clocked(self, q_draft, stream=None):
         """predict() with the step taken from (and advanced in) self.clock."""
         ob.oasis_score_blocks(self.cfg, q_draft, self.summ, self.scores, stream)

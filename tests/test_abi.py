@@ -114,6 +114,12 @@ def test_entry_points_reject_bad_arguments_before_launch(lib):
     assert L.oasis_score_blocks_minmax(C.byref(wide), ok, ok, ok, null) == ob.OASIS_ERR_UNSUPPORTED
     assert L.oasis_score_blocks_minmax(C.byref(c), odd, ok, ok, null) == ob.OASIS_ERR_INVALID_ARG
     assert L.oasis_build_summaries_minmax(C.byref(c), ok, odd, null) == ob.OASIS_ERR_INVALID_ARG
+    # the one-launch prediction chain: at most 256 slots / top-K
+    big = ob.OasisConfig.make(dict(W.TINY.config(), kv_budget_tokens=16 * 300, top_k=300, num_blocks=600))
+    assert L.oasis_predict_chain(C.byref(big), ok, ok, ok, 0, null, ok, ok, ok, ok, ok, ok, ok, ok, ok,
+                                 null) == ob.OASIS_ERR_UNSUPPORTED
+    assert L.oasis_predict_chain(C.byref(c), odd, ok, ok, 0, null, ok, ok, ok, ok, ok, ok, ok, ok, ok,
+                                 null) == ob.OASIS_ERR_INVALID_ARG
     bad = ob.OasisConfig.make(dict(W.TINY.config(), head_dim=64))
     assert L.oasis_score_blocks(C.byref(bad), ok, ok, ok, null) == ob.OASIS_ERR_UNSUPPORTED
     assert L.oasis_select_topk(None, ok, ok, null) == ob.OASIS_ERR_INVALID_ARG
