@@ -887,7 +887,10 @@ def gpu_arm(args):
             "growing_context": grow,
             "kernels_ms": mean_ms,
             "kernel_gbs": {k: by[k] / (mean_ms[k] * 1e-3) / 1e9 for k in kinds},
-            "gpu_launches": args.steps * 4,
+            # in the timed run: n-1 fused attention + scoring launches, the
+            # first step's attention and the last step's scoring alone, n top-K +
+            # plan and n transfer launches
+            "gpu_launches": 3 * args.steps + 1,
             "clocks": clk,
             "cpu_baseline": cpu,
             "cpu_baseline_all_cores": cpu_all,
