@@ -102,6 +102,16 @@ __device__ void topk_unit(const float* __restrict__ sc, int NB, int nblk_arg, in
                           const TopkSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T = blockDim.x;
+  // with a context length: the scores are loaded first, before anything that
+  // depends on the length, so that their loads overlap its load
+  float raw[ITEMS];
+  if constexpr (CTX) {
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+      const int j = tid + it * T;
+      raw[it] = j < NB ? __ldcg(sc + j) : 0.f;
+    }
+  }
   const int nblk = CTX ? nblk_arg : NB;  // without a context length: the whole cache
   const int a = sink < nblk ? sink : nblk;
   const int b0 = nblk - local > 0 ? nblk - local : 0;
@@ -124,7 +134,7 @@ __device__ void topk_unit(const float* __restrict__ sc, int NB, int nblk_arg, in
     const int j = tid + it * T;
     if constexpr (CTX) {
       valid[it] = j < NB && !(j < a || (j >= lo && j < nblk));
-      key[it] = valid[it] ? orderable(j < nblk ? __ldcg(sc + j) : -INFINITY) : 0u;
+      key[it] = valid[it] ? orderable(j < nblk ? raw[it] : -INFINITY) : 0u;
     } else {
       valid[it] = j < NB && !(j < a || j >= lo);
       key[it] = valid[it] ? orderable(__ldcg(sc + j)) : 0u;
