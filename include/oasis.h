@@ -344,7 +344,10 @@ oasis_status_t oasis_sparse_decode_attn_static(const oasis_config_t* cfg, const 
  * oasis_score_blocks(cfg, q_draft, summ, scores), bit for bit, with the SMs
  * shared between the two by construction ([OasisKV] Fig. 8: a layer's
  * prediction runs in the background of the following layers' compute).  The
- * two must not share output memory.  Same argument rules as the two calls. */
+ * two must not share output memory.  Same argument rules as the two calls.
+ * Launched as a programmatic dependent of the previous kernel in `stream`:
+ * it may start while that kernel finishes, and reads nothing before that
+ * kernel's results are visible, so stream order holds as for any launch. */
 oasis_status_t oasis_attend_and_score(const oasis_config_t* cfg, const uint16_t* q,
                                       const uint16_t* pool_k, const uint16_t* pool_v,
                                       const int32_t* block_of_slot, const int32_t* ctx_len,

@@ -59,6 +59,8 @@ __global__ void __launch_bounds__(SPREAD ? 32 : 1024) append_kernel(
   const int b = SPREAD ? blockIdx.x / Hkv : blockIdx.x;
   const int h = SPREAD ? blockIdx.x - b * Hkv : threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // the attention that follows may launch now (it waits for this grid's results)
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int64_t u = static_cast<int64_t>(b) * Hkv + h;
   // the token's rows do not depend on the context length: load them first
   const uint2 kn = reinterpret_cast<const uint2*>(k_new + u * kHeadDim)[lane];
