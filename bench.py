@@ -794,13 +794,19 @@ def gpu_arm(args):
         s += n_warm
         n_grow = min(args.steps, GROW_ROOM * n_inst // 2 - n_warm)
         torch.cuda.synchronize()
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record(compute)
-        run_steps(s, n_grow, grow=True)
-        g1.record(compute)
+        # timed in eight consecutive segments (one stream, no gap): the
+        # per-segment times show how the working set settles to the moving window
+        seg = [n_grow // 8] * 8
+        seg[-1] += n_grow - sum(seg)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(9)]
+        ev[0].record(compute)
+        for k, n_k in enumerate(seg):
+            run_steps(s, n_k, grow=True)
+            s += n_k
+            ev[k + 1].record(compute)
         torch.cuda.synchronize()
-        s += n_grow
-        gms = max_over_ranks(g0.elapsed_time(g1), world, dev) / n_grow
+        gms = max_over_ranks(ev[0].elapsed_time(ev[8]), world, dev) / n_grow
+        seg_us = [ev[k].elapsed_time(ev[k + 1]) / seg[k] * 1e3 for k in range(8)]
         # the append and refresh kernels alone: graphs of 8 launches over the copies
         def time_graph(fn):
             gx = torch.cuda.CUDAGraph()
@@ -829,6 +835,7 @@ def gpu_arm(args):
         grow = {"ms_per_step": gms, "value": job_throughput(world, wl.batch, gms), "unit": UNIT,
                 "vs_fixed_context_step": gms / ms_per_step, "append_ms_per_launch": append_ms,
                 "refresh_ms_per_launch": refresh_ms, "fetched_blocks_per_step": statistics.mean(gf),
+                "us_per_step_by_eighth": seg_us,
                 "ctx_start": ctx0, "ctx_end_per_copy": ctx_end, "steps": n_grow,
                 "local_blocks": layers[0].cfg.local_blocks,
                 "kernels": "append_kernel, then attn_score_kernel beside refresh_kernel; "
