@@ -60,6 +60,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-grow", action="store_true", help="skip the growing-context run")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the benchmark: the fetch-ratio x batch sweep (one JSON line per point)")
+    ap.add_argument("--sweep-batches", default="1,8,32,64")
     ap.add_argument("--profile-chain", type=int, default=0,
                     help="with --profile-steps: then this many prediction-chain launches")
     ap.add_argument("--profile-grow", action="store_true",
@@ -911,10 +914,77 @@ def gpu_arm(args):
         dist.destroy_process_group()
 
 
+def sweep_arm(args):
+    """Fetch-ratio x batch sweep on the Qwen3-8B layer shape (Tab. 2's columns:
+    GB fetched per step, host-link GB/s, HBM GB/s, tok/s).  One layer copy per
+    batch, its working set reset to the same random start for every ratio;
+    each step is the whole hot path in stream order (attention, scoring, top-K
+    + plan, transfer: no overlap between layers), timed with CUDA events after
+    an L2 flush.  Prints one JSON line per point; not the benchmark line."""
+    import torch
+    from sparse_kv_cache_oasis_gb300 import binding as ob
+    from sparse_kv_cache_oasis_gb300.layer import LayerState, bits_to_bf16
+    ob.lib()
+    dev = torch.device("cuda", 0)
+    st = torch.cuda.Stream(device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # twice the L2
+    peak, _ = measured_peaks()
+    for B in [int(x) for x in args.sweep_batches.split(",")]:
+        wl = W.sweep_point(-1.0, B)
+        qseq = W.query_sequence(wl, 0)
+        k, v = W.gen_kv(wl, 0, qseq)
+        sob, bos, lu = W.initial_resident(wl, 0)
+        L = LayerState(wl, bits_to_bf16(k), bits_to_bf16(v), sob, bos, lu, device=str(dev))
+        del k, v
+        start = [t.clone() for t in (L.slot_of_block, L.block_of_slot, L.last_used, L.pool_k, L.pool_v)]
+        qs = [tuple(bits_to_bf16(a).to(dev) for a in W.step_queries(wl, qseq, t)) for t in range(wl.steps)]
+        for ratio in W.SWEEP_RATIOS:
+            L.cfg.fetch_ratio = ratio
+            w = ob.cap_width(L.cfg)
+            for name in ("fetch_block", "fetch_slot", "evict_block"):
+                setattr(L, name, torch.full((B, wl.num_kv_heads, w), -1, dtype=torch.int32, device=dev))
+            for dst, src in zip((L.slot_of_block, L.block_of_slot, L.last_used, L.pool_k, L.pool_v), start):
+                dst.copy_(src)
+            torch.cuda.synchronize()
+            times, fetched = [], []
+            for t in range(4 + wl.steps):
+                q, qd = qs[t % wl.steps]
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(st):
+                    st.wait_stream(torch.cuda.current_stream())
+                    e0.record(st)
+                    L.attention(q, st)
+                    L.predict(qd, t, st)
+                    L.fetch(st)
+                    e1.record(st)
+                torch.cuda.synchronize()
+                if t >= 4:  # after four warm-up steps
+                    times.append(e0.elapsed_time(e1) * 1e-3)
+                    fetched.append(int(L.n_fetch.sum().item()))
+            t_step = statistics.mean(times)
+            nf = statistics.mean(fetched)
+            by = algorithmic_bytes(wl, nf, float((L.block_of_slot >= 0).sum().item()))
+            print(json.dumps({
+                "sweep": "qwen3-8b-layer ctx32k budget2k L4", "batch": B,
+                "fetch_ratio": ratio if ratio >= 0 else "all", "fetch_cap": ob.oasis_fetch_cap(L.cfg),
+                "us_per_step_serial": t_step * 1e6, "tok_s": B / t_step,
+                "gb_per_step": by["link"] / 1e9, "link_gbs": by["link"] / t_step / 1e9,
+                "hbm_gbs": by["hbm"] / t_step / 1e9, "hbm_frac_of_measured": by["hbm"] / t_step / 1e9 / peak,
+                "fetched_blocks_per_step": nf, "steps": wl.steps, "data": "synthetic"}), flush=True)
+        L.close()
+        del L, start, qs
+        torch.cuda.empty_cache()
+    assert ob.oasis_device_errors() == 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         reference_arm(args)
+        return
+    if args.sweep:
+        sweep_arm(args)
         return
     gpu_arm(args)
 
