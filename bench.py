@@ -947,7 +947,7 @@ def sweep_arm(args):
                 dst.copy_(src)
             torch.cuda.synchronize()
             times, fetched = [], []
-            for t in range(4 + wl.steps):
+            for t in range(16 + wl.steps):
                 q, qd = qs[t % wl.steps]
                 flush.zero_()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -959,7 +959,7 @@ def sweep_arm(args):
                     L.fetch(st)
                     e1.record(st)
                 torch.cuda.synchronize()
-                if t >= 4:  # after four warm-up steps
+                if t >= 16:  # after sixteen warm-up steps
                     times.append(e0.elapsed_time(e1) * 1e-3)
                     fetched.append(int(L.n_fetch.sum().item()))
             t_step = statistics.mean(times)
