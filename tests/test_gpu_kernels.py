@@ -228,6 +228,44 @@ def test_fetch_bytes_and_range_checks():
         ob.oasis_host_unregister(tv)
 
 
+@pytest.mark.parametrize("B,H,NB,S,ratio,full", [
+    (32, 8, 160, 128, -1.0, True),     # 256 units, every list full: 512 entries per CTA, 4 batches
+    (1100, 8, 6, 4, 0.5, False),       # 8800 units: more than 128 units per CTA
+    (3, 2, 64, 16, 0.2, False),        # fewer items than CTAs
+])
+def test_fetch_many_entries_and_units(B, H, NB, S, ratio, full):
+    cfg = dict(batch=B, num_q_heads=H, num_kv_heads=H, head_dim=128, block_size=16, num_blocks=NB,
+               kv_budget_tokens=16 * S, lookahead=1, top_k=S, fetch_ratio=ratio, sink_blocks=0,
+               local_blocks=0)
+    rs = np.random.default_rng(B + NB)
+    hk = rs.integers(0, 65535, size=(B, H, NB, 16, 128), dtype=np.uint16)
+    hv = rs.integers(0, 65535, size=(B, H, NB, 16, 128), dtype=np.uint16)
+    tk, tv = bits_to_bf16(hk), bits_to_bf16(hv)
+    dk, dv = ob.oasis_host_register(tk), ob.oasis_host_register(tv)
+    try:
+        w = max(oracle.fetch_cap(cfg), 1)
+        fb = np.full((B, H, w), -1, np.int32)
+        fs = np.full((B, H, w), -1, np.int32)
+        nf = (np.full((B, H), w) if full else rs.integers(0, w + 1, size=(B, H))).astype(np.int32)
+        for b in range(B):
+            for h in range(H):
+                fb[b, h, :nf[b, h]] = np.sort(rs.choice(NB, nf[b, h], replace=False))
+                fs[b, h, :nf[b, h]] = rs.choice(S, nf[b, h], replace=False)
+        pk = rs.integers(0, 65535, size=(B, H, S, 16, 128), dtype=np.uint16)
+        pv = rs.integers(0, 65535, size=(B, H, S, 16, 128), dtype=np.uint16)
+        gk, gv = dev_bits(pk), dev_bits(pv)
+        ob.oasis_fetch_blocks(cfg, dk, dv, torch.from_numpy(fb).cuda(), torch.from_numpy(fs).cuda(),
+                              torch.from_numpy(nf).cuda(), gk, gv)
+        oracle.fetch_blocks(cfg, hk, hv, fb, fs, nf, pk, pv)
+        torch.cuda.synchronize()
+        assert np.array_equal(bf16_to_bits(gk), pk) and np.array_equal(bf16_to_bits(gv), pv)
+        assert ob.oasis_device_errors() == 0
+    finally:
+        torch.cuda.synchronize()
+        ob.oasis_host_unregister(tk)
+        ob.oasis_host_unregister(tv)
+
+
 # --------------------------------------------------------------------- attention
 def _attn_case(wl, ctx_len=None, empty_frac=0.0, seed=0, scale=None):
     cfg = wl.config()
