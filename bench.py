@@ -60,6 +60,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-grow", action="store_true", help="skip the growing-context run")
+    ap.add_argument("--no-minmax-step", action="store_true", help="skip the min/max-key step run")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the benchmark: the fetch-ratio x batch sweep (one JSON line per point)")
     ap.add_argument("--sweep-batches", default="1,8,32,64")
@@ -437,7 +438,7 @@ def gpu_arm(args):
     def qset(s):
         return s % n_inst, (s // n_inst) % QUERY_SETS
 
-    def enqueue(s, active, host_io: bool, grow: bool = False):
+    def enqueue(s, active, host_io: bool, grow: bool = False, mm: bool = False):
         """Graph body of step s, a software pipeline over the layer copies as in
         Fig. 8 (each layer's prediction and transfer run in the background of
         the following layers): the attention of step s and the scoring of step
@@ -450,7 +451,8 @@ def gpu_arm(args):
         beside step s's kernels (a run's first step copies its own queries in
         before its attention).  With `grow`, step s first appends its token to
         its layer copy (cache, working set, summaries, context length) and the
-        selection uses the window at each context's end."""
+        selection uses the window at each context's end.  With `mm`, the
+        scoring runs against the min/max compressed keys."""
         fork = torch.cuda.Event()
         fork.record(compute)
         joins = []
@@ -490,15 +492,21 @@ def gpu_arm(args):
             q = q_in[i] if host_io else q_dev[i][qi]
             if fused:
                 i1, qi1 = qset(s - 1)
-                L.attention_and_score(q, layers[i1], qd_in[i1] if host_io else qd_dev[i1][qi1],
-                                      compute)
+                qd1 = qd_in[i1] if host_io else qd_dev[i1][qi1]
+                if mm:
+                    L.attention_and_score_minmax(q, layers[i1], qd1, compute)
+                else:
+                    L.attention_and_score(q, layers[i1], qd1, compute)
             else:
                 L.attention(q, compute)
         if "score" in active and not fused:
             i1, qi1 = qset(s - 1)
             qd = qd_in[i1] if host_io else qd_dev[i1][qi1]
             L1 = layers[i1]
-            branch(score_st, lambda st: ob.oasis_score_blocks(L1.cfg, qd, L1.summ, L1.scores, st))
+            if mm:
+                branch(score_st, lambda st: L1.score_minmax(qd, st))
+            else:
+                branch(score_st, lambda st: ob.oasis_score_blocks(L1.cfg, qd, L1.summ, L1.scores, st))
         if "select" in active and grow:
             L2 = layers[(s - 2) % n_inst]
             branch(select_st, lambda st: L2.select_ctx(st))
@@ -545,12 +553,12 @@ def gpu_arm(args):
     period = n_inst * QUERY_SETS
     graphs = {}
 
-    def graph_for(s, active, host_io, grow=False):
-        key = (s % period, active, host_io, grow)
+    def graph_for(s, active, host_io, grow=False, mm=False):
+        key = (s % period, active, host_io, grow, mm)
         if key not in graphs:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=compute):
-                enqueue(s, active, host_io, grow)
+                enqueue(s, active, host_io, grow, mm)
             graphs[key] = g
         return graphs[key]
 
@@ -564,17 +572,17 @@ def gpu_arm(args):
         return frozenset(("attn", "score", "select", "fetch")
                          + (("h2d_next", "d2h_prev") if host_io else ()))
 
-    def chunk_graph(s, host_io, grow=False):
-        key = ("chunk", s % period, host_io, grow)
+    def chunk_graph(s, host_io, grow=False, mm=False):
+        key = ("chunk", s % period, host_io, grow, mm)
         if key not in graphs:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=compute):
                 for k in range(CHUNK):
-                    enqueue(s + k, full_mask(host_io), host_io, grow)
+                    enqueue(s + k, full_mask(host_io), host_io, grow, mm)
             graphs[key] = g
         return graphs[key]
 
-    def run_steps(s0, n, host_io=False, grow=False):
+    def run_steps(s0, n, host_io=False, grow=False, mm=False):
         """Exactly the work of layer-steps s0..s0+n-1 (the pipeline fills in
         the first three graph steps and drains in the last three)."""
         end = s0 + n + 3
@@ -584,22 +592,22 @@ def gpu_arm(args):
             while s < end:
                 if s + CHUNK <= end and all(active_of(s + k, s0, n, host_io) == full
                                             for k in range(CHUNK)):
-                    chunk_graph(s, host_io, grow).replay()
+                    chunk_graph(s, host_io, grow, mm).replay()
                     s += CHUNK
                 else:
-                    graph_for(s, active_of(s, s0, n, host_io), host_io, grow).replay()
+                    graph_for(s, active_of(s, s0, n, host_io), host_io, grow, mm).replay()
                     s += 1
 
     # capture every graph the long runs below need, outside the timed regions,
     # and upload each to the device (a graph's first launch otherwise pays for
     # its upload, ~ms for a 16-step graph, inside whichever run launches it first)
-    def capture_all(grow):
-        for io in ((False,) if (args.no_e2e or grow) else (False, True)):
+    def capture_all(grow, mm=False):
+        for io in ((False,) if (args.no_e2e or grow or mm) else (False, True)):
             masks = {active_of(s_, 100, 50, io) for s_ in range(100, 153)}
             for s_ in range(period):
                 for m in masks:
-                    graph_for(s_, m, io, grow)
-                chunk_graph(s_, io, grow)
+                    graph_for(s_, m, io, grow, mm)
+                chunk_graph(s_, io, grow, mm)
         for g_ in graphs.values():
             upload_graph(g_, compute)
         torch.cuda.synchronize()
@@ -780,6 +788,28 @@ def gpu_arm(args):
                "h2d_bytes_per_step": q_bytes, "d2h_bytes_per_step": out_host[0].numel() * 2,
                "wall_s": wall}
 
+    # ---- the same pipelined step with the min/max compressed keys (scoring
+    # of the same bytes per block on bf16 tensor cores)
+    mm_step = None
+    if not args.no_minmax_step:
+        capture_all(False, mm=True)
+        n_warm = max(args.warmup, period + 4 * n_inst)
+        run_steps(s, n_warm, mm=True)
+        s += n_warm
+        n_mm = min(args.steps, 4000)
+        torch.cuda.synchronize()
+        m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        m0.record(compute)
+        run_steps(s, n_mm, mm=True)
+        m1.record(compute)
+        torch.cuda.synchronize()
+        s += n_mm
+        mms = max_over_ranks(m0.elapsed_time(m1), world, dev) / n_mm
+        mm_step = {"ms_per_step": mms, "value": job_throughput(world, wl.batch, mms), "unit": UNIT,
+                   "steps": n_mm, "step_roofline_frac": t_roof / (mms * 1e-3),
+                   "vs_mean_keys_step": mms / ms_per_step,
+                   "kernels": "attn_score_kernel (min/max keys) | topk_plan_kernel | fetch_kernel"}
+
     # ---- growing context: the same pipelined step with each step's token
     # appended first (cache, working set, summaries, context length) and the
     # selection's local window following the context (device-timed, like value)
@@ -894,6 +924,7 @@ def gpu_arm(args):
                 "frac_of_measured_hbm": by["chain"] / (mean_ms["chain"] * 1e-3) / 1e9 / peak,
                 "separate_launches_ms": mean_ms["score_select"],
                 "vs_separate_launches": mean_ms["chain"] / mean_ms["score_select"]},
+            "minmax_step": mm_step,
             "growing_context": grow,
             "kernels_ms": mean_ms,
             "kernel_gbs": {k: by[k] / (mean_ms[k] * 1e-3) / 1e9 for k in kinds},

@@ -354,6 +354,16 @@ oasis_status_t oasis_attend_and_score(const oasis_config_t* cfg, const uint16_t*
                                       float scale, uint16_t* out, const uint16_t* q_draft,
                                       const float* summ, float* scores, void* stream);
 
+/* oasis_attend_and_score with the min/max compressed keys:
+ * oasis_sparse_decode_attn(cfg, q, ...) and oasis_score_blocks_minmax(cfg,
+ * q_draft, summ_mm, scores) in one launch, bit for bit.  L*G <= 32. */
+oasis_status_t oasis_attend_and_score_minmax(const oasis_config_t* cfg, const uint16_t* q,
+                                             const uint16_t* pool_k, const uint16_t* pool_v,
+                                             const int32_t* block_of_slot, const int32_t* ctx_len,
+                                             float scale, uint16_t* out, const uint16_t* q_draft,
+                                             const uint16_t* summ_mm, float* scores,
+                                             void* stream);
+
 /* Joint attention of the decoded token and the L draft tokens over the same
  * working set, in one pass over its K and V ([OasisKV] Fig. 7 right: the
  * attention kernel processes the normal and the draft queries together).

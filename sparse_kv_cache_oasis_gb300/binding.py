@@ -79,6 +79,8 @@ _SIGS = {
     "oasis_refresh_summaries": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P, _P, _P, _P, _P]),
     "oasis_predict_chain": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P, C.c_int32, _P, _P, _P,
                                       _P, _P, _P, _P, _P, _P, _P, _P]),
+    "oasis_attend_and_score_minmax": (C.c_int, [C.POINTER(OasisConfig), _P, _P, _P, _P, _P,
+                                                C.c_float, _P, _P, _P, _P, _P]),
     "oasis_host_register": (C.c_int, [_P, C.c_size_t, C.POINTER(C.c_void_p)]),
     "oasis_host_unregister": (C.c_int, [_P]),
     "oasis_device_errors": (C.c_int, [C.POINTER(C.c_uint32), C.c_int32]),
@@ -447,6 +449,23 @@ def oasis_sparse_decode_attn_joint(cfg, q, q_draft, pool_k, pool_v, block_of_slo
         _ptr(pool_v, torch.bfloat16, (B, H, S, bs, D), "pool_v"),
         _ptr(block_of_slot, torch.int32, (B, H, S), "block_of_slot"), cl, float(scale),
         _ptr(out, torch.bfloat16, (B, L + 1, Hq, D), "out"), _stream(stream)))
+
+
+def oasis_attend_and_score_minmax(cfg, q, pool_k, pool_v, block_of_slot, ctx_len, scale, out,
+                                  q_draft, summ_mm, scores, stream=None) -> None:
+    """oasis_attend_and_score with min/max compressed keys (summ_mm)."""
+    c = OasisConfig.make(cfg)
+    B, H, Hq, NB, bs, D, S = _dims(c)
+    cl = None if ctx_len is None else _ptr(ctx_len, torch.int32, (B,), "ctx_len")
+    _check("oasis_attend_and_score_minmax", lib().oasis_attend_and_score_minmax(
+        C.byref(c), _ptr(q, torch.bfloat16, (B, Hq, D), "q"),
+        _ptr(pool_k, torch.bfloat16, (B, H, S, bs, D), "pool_k"),
+        _ptr(pool_v, torch.bfloat16, (B, H, S, bs, D), "pool_v"),
+        _ptr(block_of_slot, torch.int32, (B, H, S), "block_of_slot"), cl, float(scale),
+        _ptr(out, torch.bfloat16, (B, Hq, D), "out"),
+        _ptr(q_draft, torch.bfloat16, (B, c.lookahead, Hq, D), "q_draft"),
+        _ptr(summ_mm, torch.bfloat16, (B, H, NB, 2, D), "summ_mm"),
+        _ptr(scores, torch.float32, (B, H, NB), "scores"), _stream(stream)))
 
 
 def oasis_host_register(tensor: torch.Tensor) -> int:

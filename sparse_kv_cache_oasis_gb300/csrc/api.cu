@@ -508,7 +508,35 @@ oasis_status_t oasis_attend_and_score(const oasis_config_t* cfg, const uint16_t*
   if ((st = encode_pool(&tk, pool_k, s)) != OASIS_OK) return st;
   if ((st = encode_pool(&tv, pool_v, s)) != OASIS_OK) return st;
   return from_cuda(launch_attend_and_score(s, tk, tv, q, block_of_slot, ctx_len, scale, out, q_draft,
-                                           summ, scores, static_cast<cudaStream_t>(stream), di));
+                                           summ, false, scores, static_cast<cudaStream_t>(stream),
+                                           di));
+}
+
+oasis_status_t oasis_attend_and_score_minmax(const oasis_config_t* cfg, const uint16_t* q,
+                                             const uint16_t* pool_k, const uint16_t* pool_v,
+                                             const int32_t* block_of_slot, const int32_t* ctx_len,
+                                             float scale, uint16_t* out, const uint16_t* q_draft,
+                                             const uint16_t* summ_mm, float* scores,
+                                             void* stream) {
+  Shape s;
+  oasis_status_t st = make_shape(cfg, &s);
+  if (st != OASIS_OK) return st;
+  if (s.G > kMaxAttnGroup || s.L * s.G > 32) return OASIS_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return OASIS_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(pool_k, 16) || !aligned(pool_v, 16) || !aligned(out, 16) ||
+      !aligned(block_of_slot, 4))
+    return OASIS_ERR_INVALID_ARG;
+  if (ctx_len && !aligned(ctx_len, 4)) return OASIS_ERR_INVALID_ARG;
+  if (!aligned(q_draft, 16) || !aligned(summ_mm, 16) || !aligned(scores, 8))
+    return OASIS_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != OASIS_OK) return st;
+  CUtensorMap tk, tv;
+  if ((st = encode_pool(&tk, pool_k, s)) != OASIS_OK) return st;
+  if ((st = encode_pool(&tv, pool_v, s)) != OASIS_OK) return st;
+  return from_cuda(launch_attend_and_score(s, tk, tv, q, block_of_slot, ctx_len, scale, out, q_draft,
+                                           summ_mm, true, scores, static_cast<cudaStream_t>(stream),
+                                           di));
 }
 
 oasis_status_t oasis_host_register(void* host, size_t bytes, void** dev_ptr) {

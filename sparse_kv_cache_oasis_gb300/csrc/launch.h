@@ -108,8 +108,8 @@ cudaError_t launch_attend_and_score(const Shape& s, const CUtensorMap& tm_k,
                                     const CUtensorMap& tm_v, const uint16_t* q,
                                     const int32_t* block_of_slot, const int32_t* ctx_len,
                                     float scale, uint16_t* out, const uint16_t* q_draft,
-                                    const float* summ, float* scores, cudaStream_t st,
-                                    const DeviceInfo& di);
+                                    const void* summ, bool minmax, float* scores,
+                                    cudaStream_t st, const DeviceInfo& di);
 int score_ctas_per_sm();
 cudaError_t score_configure();  // one-time function attributes
 cudaError_t pred_configure();   // one-time function attributes (top-K / plan kernels)

@@ -33,12 +33,12 @@ __device__ __forceinline__ void attn_warps_barrier() {
   asm volatile("bar.sync 1, %0;\n" ::"n"(kAttnThreads) : "memory");
 }
 
-template <int MT>
-__global__ void __launch_bounds__(kFusedThreads) attn_score_kernel(
-    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+template <int MT, int KIND>
+__device__ __forceinline__ void attn_score_body(
+    const CUtensorMap* tm_k, const CUtensorMap* tm_v,
     const uint16_t* __restrict__ q, const int32_t* __restrict__ block_of_slot,
     const int32_t* __restrict__ ctx_len, float scale_log2, uint16_t* __restrict__ out,
-    const uint16_t* __restrict__ q_draft, const float* __restrict__ summ,
+    const uint16_t* __restrict__ q_draft, const float4* __restrict__ summ,
     float* __restrict__ scores, int Hq, int Hkv, int G, int S, int NB, int L, int P, int nA,
     int T, int Ra, int Rs, uint32_t* err) {
   extern __shared__ uint8_t smem_raw[];
@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kFusedThreads) attn_score_kernel(
   if (c < nA && warp < kAttnWarps) {
     const int u = c / P, b = u / Hkv, h = u - b * Hkv;
     const GroupRows rows{q, out, (static_cast<int64_t>(b) * Hq + h * G) * kHeadDim};
-    attn_cta<1>(&tm_k, &tm_v, rows, G, block_of_slot, ctx_len, scale_log2, Hkv, S, NB, P, err, smem,
+    attn_cta<1>(tm_k, tm_v, rows, G, block_of_slot, ctx_len, scale_log2, Hkv, S, NB, P, err, smem,
                 u, c % P, warp, lane, [] { attn_warps_barrier(); });
     return;
   }
@@ -72,35 +72,72 @@ __global__ void __launch_bounds__(kFusedThreads) attn_score_kernel(
   const int tpw = w_lo + qw < t_hi ? qw : t_hi - w_lo;
   float4* ring = reinterpret_cast<float4*>(smem + (attends ? kAttnSmemBody : 0)) +
                  sw * kScoreStages * 8 * 32;
-  score_warp_range<MT>(q_draft, reinterpret_cast<const float4*>(summ), scores, L, Hq, Hkv, G, NB,
-                       w_lo, tpw, ring, lane);
+  score_warp_range<MT, KIND>(q_draft, summ, scores, L, Hq, Hkv, G, NB, w_lo, tpw, ring, lane);
 }
 
-template <int MT>
+#define OASIS_FUSED_PARAMS                                                                       \
+  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,            \
+      const uint16_t *__restrict__ q, const int32_t *__restrict__ block_of_slot,                 \
+      const int32_t *__restrict__ ctx_len, float scale_log2, uint16_t *__restrict__ out,         \
+      const uint16_t *__restrict__ q_draft, const float4 *__restrict__ summ,                     \
+      float *__restrict__ scores, int Hq, int Hkv, int G, int S, int NB, int L, int P, int nA,    \
+      int T, int Ra, int Rs, uint32_t *err
+#define OASIS_FUSED_ARGS                                                                         \
+  &tm_k, &tm_v, q, block_of_slot, ctx_len, scale_log2, out, q_draft, summ, scores, Hq, Hkv, G, S, \
+      NB, L, P, nA, T, Ra, Rs, err
+
+// At most 128 registers a thread (up to 16 scoring rows, and 32 with the mean
+// keys).  With 10 warps of 128 the SM's four register banks keep room for the
+// step's top-K + plan CTA beside this one; at 130 (the 16-row min/max-key
+// instantiation uncapped) that CTA no longer fits and waits for the whole
+// launch (43 instead of 27 us per Llama layer-step).
+template <int MT, int KIND>
+__global__ void __maxnreg__(128) attn_score_kernel(OASIS_FUSED_PARAMS) {
+  attn_score_body<MT, KIND>(OASIS_FUSED_ARGS);
+}
+
+// Wider query tiles (48 or 64 rows; 32 with min/max keys, whose query
+// fragments stay unpacked): the registers they need.
+template <int MT, int KIND>
+__global__ void __launch_bounds__(kFusedThreads) attn_score_kernel_wide(OASIS_FUSED_PARAMS) {
+  attn_score_body<MT, KIND>(OASIS_FUSED_ARGS);
+}
+
+template <int MT, int KIND>
+constexpr auto fused_kernel() {
+  if constexpr (MT == 1 || (MT == 2 && KIND == kSummMean))
+    return attn_score_kernel<MT, KIND>;
+  else
+    return attn_score_kernel_wide<MT, KIND>;
+}
+
+template <int MT, int KIND>
 static cudaError_t fused_configure_mt() {
-  cudaError_t e = cudaFuncSetAttribute(attn_score_kernel<MT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const auto fn = fused_kernel<MT, KIND>();
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kFusedSmem));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_score_kernel<MT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
   return e;
 }
 
 cudaError_t fused_configure() {
-  cudaError_t e = fused_configure_mt<1>();
-  if (e == cudaSuccess) e = fused_configure_mt<2>();
-  if (e == cudaSuccess) e = fused_configure_mt<3>();
-  if (e == cudaSuccess) e = fused_configure_mt<4>();
+  cudaError_t e = fused_configure_mt<1, kSummMean>();
+  if (e == cudaSuccess) e = fused_configure_mt<2, kSummMean>();
+  if (e == cudaSuccess) e = fused_configure_mt<3, kSummMean>();
+  if (e == cudaSuccess) e = fused_configure_mt<4, kSummMean>();
+  if (e == cudaSuccess) e = fused_configure_mt<1, kSummMinMax>();
+  if (e == cudaSuccess) e = fused_configure_mt<2, kSummMinMax>();
   return e;
 }
 
-template <int MT>
+template <int MT, int KIND>
 static cudaError_t launch_fused_mt(const Shape& s, const CUtensorMap& tm_k,
                                    const CUtensorMap& tm_v, const uint16_t* q,
                                    const int32_t* block_of_slot, const int32_t* ctx_len,
                                    float scale, uint16_t* out, const uint16_t* q_draft,
-                                   const float* summ, float* scores, cudaStream_t st,
+                                   const void* summ, float* scores, cudaStream_t st,
                                    const DeviceInfo& di) {
   const int sms = di.sm_count > 0 ? di.sm_count : 148;
   const int P = attn_split(s, sms);
@@ -136,8 +173,9 @@ static cudaError_t launch_fused_mt(const Shape& s, const CUtensorMap& tm_k,
   cfg.attrs = attr;
   cfg.numAttrs = P > 1 ? 2 : 1;
   const float scale_log2 = scale * 1.4426950408889634f;
-  return cudaLaunchKernelEx(&cfg, attn_score_kernel<MT>, tm_k, tm_v, q, block_of_slot, ctx_len,
-                            scale_log2, out, q_draft, summ, scores, s.Hq, s.Hkv, s.G, s.S, s.NB,
+  return cudaLaunchKernelEx(&cfg, fused_kernel<MT, KIND>(), tm_k, tm_v, q, block_of_slot,
+                            ctx_len, scale_log2, out, q_draft, static_cast<const float4*>(summ),
+                            scores, s.Hq, s.Hkv, s.G, s.S, s.NB,
                             s.L, P, nA, static_cast<int>(T), static_cast<int>(Ra),
                             static_cast<int>(Rs), di.err);
 }
@@ -146,15 +184,23 @@ cudaError_t launch_attend_and_score(const Shape& s, const CUtensorMap& tm_k,
                                     const CUtensorMap& tm_v, const uint16_t* q,
                                     const int32_t* block_of_slot, const int32_t* ctx_len,
                                     float scale, uint16_t* out, const uint16_t* q_draft,
-                                    const float* summ, float* scores, cudaStream_t st,
-                                    const DeviceInfo& di) {
-  switch ((s.L * s.G + 15) / 16) {
-    case 1: return launch_fused_mt<1>(s, tm_k, tm_v, q, block_of_slot, ctx_len, scale, out, q_draft, summ, scores, st, di);
-    case 2: return launch_fused_mt<2>(s, tm_k, tm_v, q, block_of_slot, ctx_len, scale, out, q_draft, summ, scores, st, di);
-    case 3: return launch_fused_mt<3>(s, tm_k, tm_v, q, block_of_slot, ctx_len, scale, out, q_draft, summ, scores, st, di);
-    case 4: return launch_fused_mt<4>(s, tm_k, tm_v, q, block_of_slot, ctx_len, scale, out, q_draft, summ, scores, st, di);
-    default: return cudaErrorInvalidValue;  // rejected earlier by validation (L*G <= 64)
+                                    const void* summ, bool minmax, float* scores,
+                                    cudaStream_t st, const DeviceInfo& di) {
+  const int mt = (s.L * s.G + 15) / 16;
+#define OASIS_FUSED(M, K)                                                                        \
+  return launch_fused_mt<M, K>(s, tm_k, tm_v, q, block_of_slot, ctx_len, scale, out, q_draft,  \
+                               summ, scores, st, di)
+  if (minmax) {
+    if (mt == 1) OASIS_FUSED(1, kSummMinMax);
+    if (mt == 2) OASIS_FUSED(2, kSummMinMax);
+    return cudaErrorInvalidValue;  // rejected earlier by validation (L*G <= 32)
   }
+  if (mt == 1) OASIS_FUSED(1, kSummMean);
+  if (mt == 2) OASIS_FUSED(2, kSummMean);
+  if (mt == 3) OASIS_FUSED(3, kSummMean);
+  if (mt == 4) OASIS_FUSED(4, kSummMean);
+#undef OASIS_FUSED
+  return cudaErrorInvalidValue;  // rejected earlier by validation (L*G <= 64)
 }
 
 }  // namespace oasis

@@ -121,6 +121,12 @@ class LayerState:
                                   self.ctx_len, self.scale, self.out, q_draft, other.summ,
                                   other.scores, stream)
 
+    def attention_and_score_minmax(self, q, other, q_draft, stream=None):
+        """This layer's attention and `other` layer's min/max-key scoring in one launch."""
+        ob.oasis_attend_and_score_minmax(self.cfg, q, self.pool_k, self.pool_v, self.block_of_slot,
+                                         self.ctx_len, self.scale, self.out, q_draft, other.summ_mm,
+                                         other.scores, stream)
+
     def predict(self, q_draft, step, stream=None):
         ob.oasis_score_blocks(self.cfg, q_draft, self.summ, self.scores, stream)
         ob.oasis_select_topk(self.cfg, self.scores, self.topk, stream)
