@@ -5,9 +5,11 @@
 // compute).  The two are independent; fusing them fixes how they share the
 // SMs instead of leaving it to the block scheduler.
 //
-// GB300 design: one CTA per SM with 4 attention warps and 6 scoring warps.
+// GB300 design: one CTA per SM with 4 attention warps and 4 scoring warps
+// (measured per Llama layer-step with 3/4/5/6/7/8 scoring warps:
+// 28.1/26.0/26.5/26.9/27.3/27.4 us).
 // The attention CTAs (P per unit, in clusters of P, exactly as the attention
-// kernel) come first; the rest of the grid is scoring-only and there all ten
+// kernel) come first; the rest of the grid is scoring-only and there all eight
 // warps score.  The scoring tiles are spread evenly over the scoring warps.
 // Both roles are the bodies of the separate kernels; the attention warps
 // synchronise on named barrier 1, the scoring warps never wait for them.
@@ -21,12 +23,12 @@
 
 namespace oasis {
 
-constexpr int kFusedScoreWarps = 6;
+constexpr int kFusedScoreWarps = 4;
 constexpr int kFusedThreads = (kAttnWarps + kFusedScoreWarps) * 32;
 constexpr size_t kFusedScoreRing = static_cast<size_t>(kScoreStages) * 8 * 32 * sizeof(float4);
 constexpr size_t kFusedSmem = kAttnSmem + kFusedScoreWarps * kFusedScoreRing;
-// A scoring warp in a CTA that also attends shares its SM with the attention
-// warps and scores fewer tiles than one in a scoring-only CTA: this share.
+// Tiles of a scoring warp in a CTA that also attends, relative to one in a
+// scoring-only CTA (measured best at an equal share; 0.8 and 1.2-1.5 slower).
 constexpr double kAttendingWarpShare = 1.0;
 
 __device__ __forceinline__ void attn_warps_barrier() {
@@ -57,7 +59,7 @@ __device__ __forceinline__ void attn_score_body(
                 u, c % P, warp, lane, [] { attn_warps_barrier(); });
     return;
   }
-  // scoring warps (all ten in a scoring-only CTA): this CTA's tiles, then a
+  // scoring warps (all eight in a scoring-only CTA): this CTA's tiles, then a
   // contiguous share of them per warp
   const bool attends = c < nA;
   const int nsw = attends ? kFusedScoreWarps : kFusedScoreWarps + kAttnWarps;
@@ -87,7 +89,7 @@ __device__ __forceinline__ void attn_score_body(
       NB, L, P, nA, T, Ra, Rs, err
 
 // At most 128 registers a thread (up to 16 scoring rows, and 32 with the mean
-// keys).  With 10 warps of 128 the SM's four register banks keep room for the
+// keys).  With the CTA's warps at 128 the SM's four register banks keep room for the
 // step's top-K + plan CTA beside this one; at 130 (the 16-row min/max-key
 // instantiation uncapped) that CTA no longer fits and waits for the whole
 // launch (43 instead of 27 us per Llama layer-step).
@@ -147,8 +149,8 @@ static cudaError_t launch_fused_mt(const Shape& s, const CUtensorMap& tm_k,
   // the grid: the attention CTAs, then whole clusters of scoring-only CTAs up to one per SM
   const int C = nA < sms ? nA + (sms - nA) / P * P : nA;
   // scoring tiles per scoring warp: kAttendingWarpShare as many in a CTA that
-  // also attends (6 warps) as in a scoring-only one (10); the scoring warps
-  // are bound by their own instruction latency, not by the SM's bytes
+  // also attends (4 scoring warps) as in a scoring-only one (8); the scoring
+  // warps are bound by their own instruction latency, not by the SM's bytes
   int64_t Ra, Rs = 0;
   if (C > nA) {
     const double wa = kFusedScoreWarps * kAttendingWarpShare, ws = kFusedScoreWarps + kAttnWarps;
