@@ -11,10 +11,12 @@
  *
  *   oasis_sparse_decode_attn   attention over the working set      (Fig. 7 right)
  *   oasis_attend_and_score     attention of one layer + scoring of another in one launch (Fig. 8)
+ *     (_minmax: the same with min/max-pooled keys)
  *   oasis_sparse_decode_attn_joint  decoded + draft tokens in one pass of the working set (Fig. 7 right)
  *   oasis_score_blocks         draft queries scan compressed keys  (Fig. 7 right)
  *   oasis_score_blocks_minmax  the same against min/max-pooled keys (Fig. 7 left)
  *   oasis_select_topk          top-K blocks per KV head            (diagram step 2)
+ *     (_ctx, and oasis_predict_select_ctx: local window at each context's end)
  *   oasis_predict_chain        scoring + top-K + plan in one launch (diagram steps 2-3)
  *   oasis_plan_fetch           diff vs. working set, capped LRU    (diagram step 3, Tab. 2)
  *   oasis_fetch_blocks         host -> HBM transfer, copy stream   (diagram step 4, Fig. 8)
