@@ -446,10 +446,12 @@ def gpu_arm(args):
         and the transfer of step s-3, each on its own stream.  `active` = which of the four run (the
         first and last graphs of a run fill and drain the pipeline).  The four
         steps use four different layer copies, and each one's inputs were
-        produced by an earlier graph.  With host I/O, step s+1's queries are
+        produced by an earlier graph.  With host I/O, step s+2's queries are
         copied in from pinned host memory and step s-1's output is copied out
         beside step s's kernels (a run's first step copies its own queries in
-        before its attention).  With `grow`, step s first appends its token to
+        before its attention, and the second step's beside them): each copy has
+        two steps to land, and its destination (the buffer of a layer copy
+        last read two steps earlier) is free.  With `grow`, step s first appends its token to
         its layer copy (cache, working set, summaries, context length) and the
         selection uses the window at each context's end.  With `mm`, the
         scoring runs against the min/max compressed keys."""
@@ -472,6 +474,8 @@ def gpu_arm(args):
         if "h2d_now" in active:
             branch(h2d, lambda st: copy_in(st, s))
             compute.wait_event(joins.pop())
+        if "h2d_now1" in active:
+            branch(h2d, lambda st: copy_in(st, s + 1))
         # the attention of step s and the scoring of step s-1 share one launch
         # (oasis_attend_and_score) when both run; it is enqueued first
         fused = "attn" in active and "score" in active
@@ -520,7 +524,7 @@ def gpu_arm(args):
             L3 = layers[(s - 3) % n_inst]
             branch(copy, lambda st: L3.fetch(st))
         if "h2d_next" in active:
-            branch(h2d, lambda st: copy_in(st, s + 1))
+            branch(h2d, lambda st: copy_in(st, s + 2))
         if "d2h_prev" in active:
             ip = (s - 1) % n_inst
 
@@ -539,7 +543,9 @@ def gpu_arm(args):
         if host_io:
             if s == s0:
                 parts.append("h2d_now")
-            if s0 <= s + 1 < s0 + n:
+                if n > 1:
+                    parts.append("h2d_now1")
+            if s0 <= s + 2 < s0 + n:
                 parts.append("h2d_next")
             if s0 <= s - 1 < s0 + n:
                 parts.append("d2h_prev")
