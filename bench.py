@@ -593,6 +593,9 @@ def gpu_arm(args):
         the first three graph steps and drains in the last three)."""
         end = s0 + n + 3
         full = full_mask(host_io)
+        torch.cuda.nvtx.range_push(f"layer-steps {s0}..{s0 + n - 1}"
+                                   + (" host-io" if host_io else "") + (" grow" if grow else "")
+                                   + (" minmax" if mm else ""))
         with torch.cuda.stream(compute):
             s = s0
             while s < end:
@@ -603,6 +606,7 @@ def gpu_arm(args):
                 else:
                     graph_for(s, active_of(s, s0, n, host_io), host_io, grow, mm).replay()
                     s += 1
+        torch.cuda.nvtx.range_pop()
 
     # capture every graph the long runs below need, outside the timed regions,
     # and upload each to the device (a graph's first launch otherwise pays for

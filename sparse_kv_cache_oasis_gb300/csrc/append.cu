@@ -22,7 +22,9 @@
 // per request).  The context length is read by every warp before one cluster
 // barrier and advanced after it.  The victim search is a warp-wide minimum
 // over 64-bit keys (class, last use, block id); rows copied into a newly
-// taken slot are all loaded before any is stored.  The exact mean needs
+// taken slot are loaded eight at a time before they are stored.  The
+// attention that follows is a programmatic dependent: it may launch while
+// this grid runs and waits for its results.  The exact mean needs
 // double arithmetic, which GB300 runs at a small fraction of its fp32 rate
 // (one CTA per request with the mean inside took ~8 us); the refresh runs it
 // one warp per SM on a stream beside the attention.

@@ -193,6 +193,7 @@ class LayerState:
         `fetch_done`."""
         compute = compute or torch.cuda.current_stream()
         copy = copy or compute
+        torch.cuda.nvtx.range_push(f"oasis layer-step {step}")
         compute.wait_event(self.fetch_done)
         self.attention(q, compute)
         self.predict(q_draft, step, compute)
@@ -201,6 +202,7 @@ class LayerState:
         copy.wait_event(planned)
         self.fetch(copy)
         self.fetch_done.record(copy)
+        torch.cuda.nvtx.range_pop()
         return self.out
 
     def close(self):
@@ -220,3 +222,34 @@ class LayerState:
     def state_numpy(self):
         return (self.slot_of_block.cpu().numpy(), self.block_of_slot.cpu().numpy(),
                 self.last_used.cpu().numpy())
+
+    _STATE = ("slot_of_block", "block_of_slot", "last_used", "clock", "pool_k", "pool_v", "summ")
+
+    def dump(self, path):
+        """Writes the layer's device state (working-set maps, LRU times, step
+        clock, pools, summaries, context lengths) to an .npz file, e.g. to
+        replay a step on the oracle from exactly this state."""
+        arrays = {}
+        for name in self._STATE:
+            t = getattr(self, name).detach().cpu().contiguous()
+            arrays[name] = t.view(torch.int16).numpy() if t.dtype == torch.bfloat16 else t.numpy()
+        if self.ctx_len is not None:
+            arrays["ctx_len"] = self.ctx_len.cpu().numpy()
+        np.savez(path, **arrays)
+
+    def restore(self, path):
+        """Loads a state written by dump() into this layer's buffers (same shapes)."""
+        with np.load(path) as z:
+            for name in self._STATE:
+                dst = getattr(self, name)
+                src = torch.from_numpy(z[name])
+                if dst.dtype == torch.bfloat16:
+                    src = src.view(torch.bfloat16)
+                if tuple(src.shape) != tuple(dst.shape):
+                    raise ValueError(f"{name}: shape {tuple(src.shape)} in {path}, expected {tuple(dst.shape)}")
+                dst.copy_(src)
+            if "ctx_len" in z.files:
+                if self.ctx_len is None:
+                    self.ctx_len = torch.from_numpy(z["ctx_len"]).to(self.summ.device)
+                else:
+                    self.ctx_len.copy_(torch.from_numpy(z["ctx_len"]))

@@ -112,3 +112,29 @@ def test_sweep_points_fetch_volume(ratio):
     if ratio > 0:
         # the capped transfer is saturated at step 0 (random initial working set)
         assert fetched[0] == cap * wl.batch * wl.num_kv_heads
+
+
+def test_state_dump_and_restore_replays_a_step(tmp_path):
+    """A layer's device state written by dump() and loaded by restore() makes
+    the next step repeat bit for bit (the state of a parity repro)."""
+    wl = W.TINY.with_(steps=3)
+    st, k, v, qseq = setup_layer(wl)
+    q0, qd0 = W.step_queries(wl, qseq, 0)
+    st.step(0, dev_bits(q0), dev_bits(qd0))
+    torch.cuda.synchronize()
+    path = tmp_path / "state.npz"
+    st.dump(path)
+    q1, qd1 = W.step_queries(wl, qseq, 1)
+    st.step(1, dev_bits(q1), dev_bits(qd1))
+    torch.cuda.synchronize()
+    after = [t.clone() for t in (st.out, st.topk, st.slot_of_block, st.block_of_slot, st.last_used,
+                                 st.pool_k, st.pool_v)]
+    st.restore(path)
+    st.step(1, dev_bits(q1), dev_bits(qd1))
+    torch.cuda.synchronize()
+    again = (st.out, st.topk, st.slot_of_block, st.block_of_slot, st.last_used, st.pool_k, st.pool_v)
+    for a, b in zip(after, again):
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b)
+    assert ob.oasis_device_errors() == 0
+    st.close()
