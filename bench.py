@@ -19,8 +19,17 @@ s-1, top-K + plan of copy s-2 and the transfer of copy s-3 (a software
 pipeline over layers); the LRU step lives in device memory, so replays
 advance it.
 
-Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the
-same workload instead.
+Prints one JSON line (rank 0).  Beside the headline (`value`, `roofline` of
+the fused attention + scoring launch, `step_roofline`, `e2e` with the
+queries copied in and the output copied out every step, `cpu_baseline`,
+`clocks`), it carries each kernel timed alone (`kernels_ms`) and the rows
+beyond the hot path, each on the same layer: `joint_attention` (decoded and
+draft tokens in one KV pass), `minmax_scoring` and `minmax_step` (min/max
+compressed keys), `predict_chain` (scoring + top-K + plan in one launch) and
+`growing_context` (a token appended per step, the local window following the
+context).  --impl reference times the CPU oracle on the same workload
+instead; --sweep runs the fetch-ratio x batch sweep on the Qwen3-8B layer
+shape (one JSON line per point, not the benchmark line).
 """
 from __future__ import annotations
 
