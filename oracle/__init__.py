@@ -12,6 +12,10 @@ with the fields of ``orc_cfg``.
 Method source: "OasisKV: Scaling In-Decode KV Cache Beyond HBM with Lookahead
 Sparse Prefetching" (arXiv:2608.08097 summary page); each C function cites the
 figure, table or step of the page it follows.
+
+Parity unpinned: multi-step trajectories (``Stepper`` run over many steps).
+Each step's functions are pinned on their own; the page prints no trajectory
+that would pin the chain of steps as a whole.
 """
 from __future__ import annotations
 
@@ -337,7 +341,8 @@ class Stepper:
     q_t, then scoring with the draft queries, top-K, planning at step t and
     the transfer that produces the next working set ([OasisKV] Fig. 8: the
     draft query of step t drives prediction, selection and transfer before
-    the same layer's attention at step t+1).
+    the same layer's attention at step t+1).  Parity unpinned over many
+    steps: only the per-step functions it calls are pinned.
     """
 
     def __init__(self, cfg, host_k, host_v, summ, slot_of_block, block_of_slot, last_used,

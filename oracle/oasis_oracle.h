@@ -11,6 +11,11 @@
  * HBM with Lookahead Sparse Prefetching" (arXiv:2608.08097, summary page that
  * carries the paper's figure and table captions).
  *
+ * Every function here is pinned by the CPU tests to hand-computed cases,
+ * closed forms, brute force or invariants.  Parity unpinned: multi-step
+ * trajectories (the functions chained over many steps); the page prints
+ * none.
+ *
  * Layouts (row-major, all sizes in elements):
  *   K, V (host full cache) : [B][Hkv][NB][bs][D]      bf16 bit patterns
  *   summ                   : [B][Hkv][NB][D]          fp32
