@@ -30,11 +30,15 @@
 // queries there, and leaves the SM's shared-memory bandwidth to the attention
 // kernel running beside it.
 // Balance: the tiles of 8 consecutive blocks of all (request, KV head) units
-// form one list of T tiles; CTA c (one per SM) takes the contiguous range
-// [c*Rt, (c+1)*Rt) and each warp a contiguous eighth of it, so every SM
-// streams the same number of bytes whatever NB and the unit count, a warp
-// reloads its query fragments only where its tiles cross into the next unit,
-// and one CTA per SM leaves room for the attention kernel's CTA beside it.
+// form one list of T tiles; CTA c (two per SM) takes the contiguous range
+// [c*Rt, (c+1)*Rt) and each warp a contiguous sixth of it, so every SM
+// streams the same number of bytes whatever NB and the unit count, and a
+// warp reloads its query fragments only where its tiles cross into the next
+// unit.  Two CTAs per SM (72 KiB of rings each) took 16.4 us at the Llama
+// layer against 18.9 us for one: the kernel is bound by each warp's latency
+// per tile, and twice the warps hide more of it.  A caller that wants the
+// attention and the scoring at once uses the fused launch (stream.cu), which
+// shares every SM between the two roles.
 #include "launch.h"
 #include "score_body.cuh"
 
@@ -43,6 +47,7 @@ namespace oasis {
 constexpr int kScoreThreads = 192;
 constexpr int kScoreWarps = kScoreThreads / 32;
 constexpr int kMinTilesPerCta = 16;
+constexpr int kScoreCtasPerSm = 2;  // resident CTAs of this kernel per SM
 
 template <int MT, int KIND>
 __global__ void __launch_bounds__(kScoreThreads) score_kernel(
@@ -69,10 +74,10 @@ static size_t score_smem_bytes(int) {
 template <int MT, int KIND>
 static cudaError_t launch_mt(const Shape& s, const uint16_t* q_draft, const void* summ,
                              float* scores, cudaStream_t st, const DeviceInfo& di) {
-  // one CTA per SM over equal contiguous tile ranges
+  // kScoreCtasPerSm CTAs per SM over equal contiguous tile ranges
   const int ntiles = (s.NB + 7) / 8;
   const int64_t T = static_cast<int64_t>(s.units()) * ntiles;
-  int64_t C = di.sm_count > 0 ? di.sm_count : 148;
+  int64_t C = static_cast<int64_t>(kScoreCtasPerSm) * (di.sm_count > 0 ? di.sm_count : 148);
   const int64_t cap = (T + kMinTilesPerCta - 1) / kMinTilesPerCta;
   if (C > cap) C = cap;
   if (C < 1) C = 1;
