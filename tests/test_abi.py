@@ -134,3 +134,32 @@ def test_binding_checks_tensors(lib):
     with pytest.raises(TypeError):
         ob.oasis_select_topk(wl, torch.zeros(1, 4, 256, dtype=torch.float64),
                              torch.zeros(1, 4, 32, dtype=torch.int32))
+
+
+def test_header_layout_and_constants_match_the_binding(tmp_path):
+    """A C program built against include/oasis.h prints the struct layout, the
+    status codes and the device error bits; the ctypes binding must agree."""
+    fields = [n for n, _ in ob.OasisConfig._fields_]
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "oasis.h"', 'int main(void) {',
+             '  printf("sizeof %zu\\n", sizeof(oasis_config_t));']
+    lines += [f'  printf("off_{n} %zu\\n", offsetof(oasis_config_t, {n}));' for n in fields]
+    status = ["OASIS_OK", "OASIS_ERR_INVALID_ARG", "OASIS_ERR_UNSUPPORTED", "OASIS_ERR_CUDA",
+              "OASIS_ERR_TIMEOUT"]
+    deverr = ["FETCH_RANGE", "PLAN_STATE", "TOPK_IDS", "WAIT_TIMEOUT", "SLOT_RANGE", "CTX_FULL",
+              "NO_SLOT"]
+    lines += [f'  printf("{s} %d\\n", (int){s});' for s in status]
+    lines += [f'  printf("DEVERR_{d} %u\\n", (unsigned)OASIS_DEVERR_{d});' for d in deverr]
+    lines += ['  return 0;', '}']
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-std=c11", "-Wall", "-Werror", "-I",
+                           os.path.dirname(ob.HEADER), str(src), "-o", str(exe)])
+    got = dict(line.split() for line in subprocess.check_output([str(exe)], text=True).splitlines())
+    assert int(got["sizeof"]) == C.sizeof(ob.OasisConfig)
+    for n in fields:
+        assert int(got[f"off_{n}"]) == getattr(ob.OasisConfig, n).offset, n
+    for s in status:
+        assert int(got[s]) == getattr(ob, s), s
+    for d in deverr:
+        assert int(got[f"DEVERR_{d}"]) == getattr(ob, f"DEVERR_{d}"), d
