@@ -58,6 +58,16 @@ MUTANTS = {
     "attention drops the scale": ("double w = exp(x * scale - mx);", "double w = exp(x - mx);"),
     "attention mask off by one": ("(int64_t)j * bs + t >= ctx_len[b]", "(int64_t)j * bs + t > ctx_len[b]", "all"),
     "attention GQA index transposed": ("const int hq = h * G + g;", "const int hq = g * H + h;"),
+    "attention skips the normalisation": ("o[d] = den > 0.0 ? (float)(acc[d] / den) : 0.0f;",
+                                          "o[d] = den > 0.0 ? (float)(acc[d]) : 0.0f;"),
+    "plan evicts one block too many": ("e = nres + n - S;", "e = nres + n - S + 1;"),
+    "plan evicts though slots are empty": ("e = nres + n - S;", "e = n;"),
+    "fetched blocks not marked used": ("                sob[fetched[r]] = s;\n                lu[s] = step;",
+                                       "                sob[fetched[r]] = s;"),
+    "free slots taken from the top": ("for (int s = 0; s < S; ++s) {\n                int free_slot",
+                                      "for (int s = S - 1; s >= 0; --s) {\n                int free_slot"),
+    "refresh reads the whole block": ("for (int r = 0; r <= t; ++r) {\n                    sum +=",
+                                      "for (int r = 0; r < bs; ++r) {\n                    sum +="),
 }
 
 
