@@ -366,7 +366,8 @@ _uploaded = set()
 
 def upload_graph(g, stream):
     """Uploads an instantiated CUDA graph to the device ahead of its first
-    launch (driver cuGraphUpload on the graph's executable), once per graph;
+    launch (the CUDA driver API's cuGraphUpload on the graph's executable),
+    once per graph;
     a no-op where the executable is not exposed."""
     import ctypes
     get = getattr(g, "raw_cuda_graph_exec", None)
