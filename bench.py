@@ -367,8 +367,7 @@ _uploaded = set()
 def upload_graph(g, stream):
     """Uploads an instantiated CUDA graph to the device ahead of its first
     launch (the CUDA driver API's cuGraphUpload on the graph's executable),
-    once per graph;
-    a no-op where the executable is not exposed."""
+    once per graph; a no-op where the executable is not exposed."""
     import ctypes
     get = getattr(g, "raw_cuda_graph_exec", None)
     if get is None or id(g) in _uploaded:
