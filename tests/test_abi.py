@@ -163,3 +163,16 @@ def test_header_layout_and_constants_match_the_binding(tmp_path):
         assert int(got[s]) == getattr(ob, s), s
     for d in deverr:
         assert int(got[f"DEVERR_{d}"]) == getattr(ob, f"DEVERR_{d}"), d
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the behaviour without a device")
+def test_without_a_device_waits_and_queries_fail_fast(lib):
+    """No device: the bounded stream wait and the error-word query return
+    OASIS_ERR_CUDA at once instead of waiting or reporting success."""
+    import time
+    t0 = time.monotonic()
+    assert ob.oasis_stream_wait(0, 2000) == ob.OASIS_ERR_CUDA
+    assert time.monotonic() - t0 < 1.0
+    with pytest.raises(ob.OasisError) as e:
+        ob.oasis_device_errors()
+    assert e.value.status == ob.OASIS_ERR_CUDA
